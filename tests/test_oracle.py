@@ -1,0 +1,277 @@
+"""Pins for the float64 CPU oracle (no GPU).
+
+The oracle is checked against facts fixed outside itself: hand-worked closed
+forms (tests/golden), invariances of the softmax, special cases with a known
+answer, the tile-by-tile online recurrence, and an independent float64 library
+implementation.  Each test names the mistake it is there to catch.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_attn_fwd_05_gb300.inputs import make_qkv, make_rows
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "attention_closed_forms.json")
+
+
+def _ev(expr: str) -> float:
+    """Evaluate a closed-form expression over e, log and integers."""
+    return float(eval(expr, {"__builtins__": {}}, {"e": math.e, "log": math.log}))
+
+
+def _qkv(B, H, N, d, seed, dist="normal"):
+    q, k, v = make_qkv(B, H, N, d, seed, "f32", dist)
+    return q.numpy(), k.numpy(), v.numpy()
+
+
+# ---------------------------------------------------------------- golden ---
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_golden_closed_forms(causal):
+    """Hand-worked examples: catches a dropped scale, a transposed S, a wrong
+    causal boundary and a wrong LSE base."""
+    g = json.load(open(GOLDEN))
+    for case in g["cases"]:
+        q = np.array(case["q"], np.float32)[None, None]
+        k = np.array(case["k"], np.float32)[None, None]
+        v = np.array(case["v"], np.float32)[None, None]
+        o, lse = oracle.attn_fwd(q, k, v, case["scale"], causal)
+        ko, kl = ("o_causal", "lse_causal") if causal else ("o", "lse")
+        want_o = np.array([[_ev(x) for x in row] for row in case[ko]])
+        want_l = np.array([_ev(x) for x in case[kl]])
+        np.testing.assert_allclose(o[0, 0], want_o, rtol=0, atol=1e-14, err_msg=case["name"])
+        np.testing.assert_allclose(lse[0, 0], want_l, rtol=0, atol=1e-14, err_msg=case["name"])
+
+
+def test_golden_online_two_tiles():
+    """The two-tile online normalisation example, worked by hand."""
+    g = json.load(open(GOLDEN))["online_two_tiles"]
+    # One query row, d = 1, q = 1, scale = 1: the logits are the key values.
+    x = np.array(g["logits"], np.float32)
+    N = x.shape[0]
+    q = np.ones((N, 1), np.float32)
+    k = x.reshape(N, 1)
+    v = np.ones((N, 1), np.float32)  # O = 1 exactly; LSE carries m and d
+    _, lse_t = oracle.online_replay(q, k, v, 1.0, False, tile=len(g["tiles"][0]))
+    m, d = _ev(g["m_final"]), _ev(g["d_final"])
+    assert abs(lse_t[0] - (m + math.log(d))) < 1e-14
+    _, lse_1 = oracle.online_replay(q[:2], k[:2], v[:2], 1.0, False, tile=2)
+    m1, d1 = _ev(g["m_after_tile1"]), _ev(g["d_after_tile1"])
+    assert abs(lse_1[0] - (m1 + math.log(d1))) < 1e-14
+
+
+# ------------------------------------------------------------ T1 one key ---
+
+def test_t1_single_key_returns_v():
+    """N = 1: softmax of one logit is 1, so O = V[0] and LSE = scale*q.k."""
+    q, k, v = _qkv(2, 3, 1, 16, 10)
+    scale = 0.37
+    o, lse = oracle.attn_fwd(q, k, v, scale, False)
+    np.testing.assert_array_equal(o, v.astype(np.float64))
+    want = scale * np.einsum("bhnd,bhnd->bhn", q.astype(np.float64), k.astype(np.float64))
+    np.testing.assert_allclose(lse, want, rtol=1e-15, atol=1e-15)
+
+
+def test_t1_causal_first_row_returns_v0():
+    """Causal row 0 sees key 0 only, for any N (catches an off-by-one mask)."""
+    q, k, v = _qkv(1, 2, 37, 8, 11)
+    o, lse = oracle.attn_fwd(q, k, v, 0.5, True)
+    np.testing.assert_array_equal(o[:, :, 0], v[:, :, 0].astype(np.float64))
+    want = 0.5 * (q[:, :, 0].astype(np.float64) * k[:, :, 0]).sum(-1)
+    np.testing.assert_allclose(lse[:, :, 0], want, rtol=1e-15, atol=1e-15)
+
+
+# ------------------------------------------------------- T2 uniform scores ---
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_t2_zero_queries_average_v(causal):
+    """Q = 0 makes every logit 0: O = mean of the visible V rows, LSE = ln(#visible)."""
+    _, k, v = _qkv(1, 2, 50, 8, 12)
+    q = np.zeros_like(k)
+    o, lse = oracle.attn_fwd(q, k, v, 1.0, causal)
+    v64 = v.astype(np.float64)
+    N = v.shape[2]
+    if causal:
+        counts = np.arange(1, N + 1, dtype=np.float64)
+        want_o = np.cumsum(v64, axis=2) / counts[None, None, :, None]
+        want_l = np.broadcast_to(np.log(counts), lse.shape)
+    else:
+        want_o = np.broadcast_to(v64.mean(axis=2, keepdims=True), o.shape)
+        want_l = np.full(lse.shape, math.log(N))
+    np.testing.assert_allclose(o, want_o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, want_l, rtol=0, atol=1e-13)
+
+
+def test_t2_equal_keys_average_v():
+    """All K rows equal: scores are constant per row, so O = mean(V) for any Q,
+    and LSE = scale*q.k + ln N."""
+    q, k, v = _qkv(1, 1, 40, 8, 13)
+    k = np.broadcast_to(k[:, :, :1], k.shape).copy()
+    o, lse = oracle.attn_fwd(q, k, v, 0.3, False)
+    np.testing.assert_allclose(o, np.broadcast_to(v.astype(np.float64).mean(2, keepdims=True),
+                                                  o.shape), rtol=1e-12, atol=1e-13)
+    s = 0.3 * (q.astype(np.float64) * k[:, :, :1].astype(np.float64)).sum(-1)
+    np.testing.assert_allclose(lse, s + math.log(40), rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------- T3 shift invariance ---
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_t3_key_shift_changes_lse_only(causal):
+    """K' = K + 1 u^T shifts row i's logits by scale*q_i.u: O is unchanged and
+    LSE moves by exactly that amount (catches a missing max-subtraction term
+    or a wrong LSE)."""
+    q, k, v = _qkv(1, 2, 33, 8, 14)
+    # u on a coarse grid keeps K + u exact in float32.
+    u = np.array([0.5, -1.0, 0.25, 2.0, 0.0, -0.75, 1.5, -0.5], np.float32)
+    k = np.round(k * 64) / 64
+    k2 = (k + u).astype(np.float32)
+    assert np.array_equal(k2 - u, k)  # exact
+    scale = 0.25
+    o1, l1 = oracle.attn_fwd(q, k, v, scale, causal)
+    o2, l2 = oracle.attn_fwd(q, k2, v, scale, causal)
+    np.testing.assert_allclose(o2, o1, rtol=1e-11, atol=1e-12)
+    shift = scale * (q.astype(np.float64) @ u.astype(np.float64))
+    np.testing.assert_allclose(l2, l1 + shift, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- T4 permutation ---
+
+def test_t4_permuting_keys_and_values_together():
+    """Non-causal: permuting K and V rows together leaves O and LSE unchanged;
+    permuting V alone does not (catches K/V pairing mistakes)."""
+    q, k, v = _qkv(2, 2, 29, 8, 15)
+    perm = np.random.default_rng(0).permutation(29)
+    o1, l1 = oracle.attn_fwd(q, k, v, 0.35, False)
+    o2, l2 = oracle.attn_fwd(q, k[:, :, perm], v[:, :, perm], 0.35, False)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, rtol=1e-13, atol=1e-13)
+    o3, _ = oracle.attn_fwd(q, k, v[:, :, perm], 0.35, False)
+    assert np.abs(o3 - o1).max() > 1e-3
+
+
+# -------------------------------------------------------- T5 row sums ---
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_t5_probability_rows(causal):
+    """Each row of P sums to 1, masked keys get 0, and P @ V gives O."""
+    q, k, v = _qkv(1, 1, 45, 8, 16)
+    o, _ = oracle.attn_fwd(q, k, v, 0.4, causal)
+    for i in (0, 1, 17, 44):
+        p = oracle.probs_row(q[0, 0], k[0, 0], i, 0.4, causal)
+        assert abs(p.sum() - 1.0) < 1e-12
+        assert (p >= 0).all()
+        if causal:
+            assert (p[i + 1:] == 0).all() and (p[:i + 1] > 0).all()
+        np.testing.assert_allclose(p @ v[0, 0].astype(np.float64), o[0, 0, i],
+                                   rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------- T6 online replay ---
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(16, 8), (13, 4), (7, 2)])
+def test_t6_online_replay_matches_one_shot(N, d, causal):
+    """The tile-by-tile recurrence equals the one-shot softmax for any tile size."""
+    q, k, v = _qkv(1, 1, N, d, 17 + N, "stress")
+    o, lse = oracle.attn_fwd(q, k, v, 1.0 / math.sqrt(d), causal)
+    for tile in sorted({1, 2, max(1, N // 2), N}):
+        ot, lt = oracle.online_replay(q[0, 0], k[0, 0], v[0, 0], 1.0 / math.sqrt(d), causal, tile)
+        np.testing.assert_allclose(ot, o[0, 0], rtol=1e-12, atol=1e-12, err_msg=f"tile={tile}")
+        np.testing.assert_allclose(lt, lse[0, 0], rtol=1e-12, atol=1e-12, err_msg=f"tile={tile}")
+
+
+# ------------------------------------------------------ T7 brute force ---
+
+def test_t7_two_keys_sigmoid_form():
+    """N = 2, d = 1: O = sigma(s0 - s1) v0 + sigma(s1 - s0) v1 and
+    LSE = logaddexp(s0, s1), for random small inputs."""
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        q = rng.standard_normal((1, 1, 2, 1)).astype(np.float32)
+        k = rng.standard_normal((1, 1, 2, 1)).astype(np.float32)
+        v = rng.standard_normal((1, 1, 2, 1)).astype(np.float32)
+        scale = float(rng.uniform(0.1, 2.0))
+        o, lse = oracle.attn_fwd(q, k, v, scale, False)
+        for i in range(2):
+            s0 = scale * float(q[0, 0, i, 0]) * float(k[0, 0, 0, 0])
+            s1 = scale * float(q[0, 0, i, 0]) * float(k[0, 0, 1, 0])
+            sig = 1.0 / (1.0 + math.exp(s1 - s0))
+            want = sig * float(v[0, 0, 0, 0]) + (1 - sig) * float(v[0, 0, 1, 0])
+            assert abs(o[0, 0, i, 0] - want) < 1e-14
+            assert abs(lse[0, 0, i] - np.logaddexp(s0, s1)) < 1e-14
+
+
+# -------------------------------------------------- T8 library cross-check ---
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dist", ["normal", "stress"])
+def test_t8_matches_float64_library_sdpa(causal, dist):
+    """An independent float64 implementation (PyTorch's math SDPA and
+    logsumexp on the CPU) agrees to 1e-12 on the same seeded inputs."""
+    qt, kt, vt = make_qkv(2, 3, 67, 16, 18, "bf16", dist)
+    scale = 0.25
+    o, lse = oracle.attn_fwd(qt, kt, vt, scale, causal)
+    q64, k64, v64 = (t.to(torch.float64) for t in (qt, kt, vt))
+    ref = torch.nn.functional.scaled_dot_product_attention(q64, k64, v64, is_causal=causal,
+                                                           scale=scale)
+    s = scale * q64 @ k64.transpose(-1, -2)
+    if causal:
+        N = s.shape[-1]
+        s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    ref_lse = torch.logsumexp(s, dim=-1)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- sampled rows ---
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_subset_matches_full(causal):
+    q, k, v = _qkv(2, 2, 40, 8, 19)
+    o, lse = oracle.attn_fwd(q, k, v, 0.3, causal)
+    bh = np.array([0, 1, 2, 3, 3, 0])
+    rows = np.array([0, 39, 17, 5, 0, 38])
+    ro, rl = oracle.attn_fwd_rows(q, k, v, 0.3, causal, bh, rows)
+    of = o.reshape(4, 40, 8)
+    lf = lse.reshape(4, 40)
+    np.testing.assert_array_equal(ro, of[bh, rows])
+    np.testing.assert_array_equal(rl, lf[bh, rows])
+
+
+def test_rows_subset_rejects_bad_index():
+    q, k, v = _qkv(1, 1, 4, 2, 20)
+    with pytest.raises(RuntimeError):
+        oracle.attn_fwd_rows(q, k, v, 1.0, False, [0], [4])
+
+
+def test_oracle_threads_do_not_change_result():
+    q, k, v = _qkv(1, 2, 64, 8, 21)
+    o1, l1 = oracle.attn_fwd(q, k, v, 0.3, True, nthreads=1)
+    o4, l4 = oracle.attn_fwd(q, k, v, 0.3, True, nthreads=4)
+    np.testing.assert_array_equal(o1, o4)
+    np.testing.assert_array_equal(l1, l4)
+
+
+# ------------------------------------------------------- row softmax ---
+
+def test_row_softmax_closed_forms_and_library():
+    """Constant rows give 1/width; a row [0, ln-free ints] matches e-powers;
+    random rows match torch.softmax in float64."""
+    x = np.zeros((2, 5), np.float32)
+    x[1] = [0, 1, 2, 3, 4]
+    y, lse = oracle.row_softmax(x)
+    np.testing.assert_allclose(y[0], 0.2, rtol=0, atol=1e-16)
+    z = sum(math.e ** j for j in range(5))
+    np.testing.assert_allclose(y[1], [math.e ** j / z for j in range(5)], rtol=1e-15, atol=0)
+    assert abs(lse[1] - math.log(z)) < 1e-14
+    xr = make_rows(7, 300, 5, spread=8.0).numpy()
+    y, lse = oracle.row_softmax(xr)
+    xt = torch.from_numpy(xr).to(torch.float64)
+    np.testing.assert_allclose(y, torch.softmax(xt, -1).numpy(), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse, torch.logsumexp(xt, -1).numpy(), rtol=1e-13, atol=1e-13)
