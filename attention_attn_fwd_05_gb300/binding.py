@@ -1,0 +1,228 @@
+"""Thin ctypes binding over the C ABI in ``include/attn_fwd.h``.
+
+Argument marshalling only: shape, dtype, device and contiguity checks raise
+``ValueError`` (the pages' wrapper convention), output tensors are allocated
+with PyTorch, and every step of the computation runs in the CUDA library.
+There is no fallback: if the library is missing or the device is not sm_103,
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from .build import LIB
+
+ATTN_F32, ATTN_BF16 = 0, 1
+STATUS_NAMES = {
+    0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_DTYPE",
+    4: "ATTN_ERR_HEADDIM", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_ARCH", 7: "ATTN_ERR_LAUNCH",
+    8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
+}
+EXPORTED = ("attn_fwd", "attn_row_softmax", "attn_device_status",
+            "attn_selftest_wait_timeout", "attn_status_string", "attn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-OK status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        name = STATUS_NAMES.get(self.status, str(status))
+        msg = lib().attn_status_string(self.status).decode()
+        super().__init__(f"{where}: {name} ({msg})")
+
+
+def lib():
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB):
+            raise RuntimeError(
+                f"CUDA library not built ({LIB} missing): run __graft_entry__.build() "
+                "or python -m attention_attn_fwd_05_gb300.build")
+        L = ctypes.CDLL(LIB)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                               ctypes.c_int, ctypes.c_int, vp]
+        L.attn_row_softmax.argtypes = [vp, vp, vp, i64, i64, vp]
+        L.attn_device_status.argtypes = [vp]
+        L.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.attn_status_string.argtypes = [ctypes.c_int]
+        L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_version.argtypes = []
+        for name in ("attn_fwd", "attn_row_softmax", "attn_device_status",
+                     "attn_selftest_wait_timeout", "attn_version"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise AttnError(status, where)
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return ATTN_F32
+    if t == torch.bfloat16:
+        return ATTN_BF16
+    raise ValueError(f"attn_fwd supports float32 and bfloat16 tensors, got {t}")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+             causal: bool = False, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+             stream: Optional[torch.cuda.Stream] = None
+             ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """O = softmax(scale * Q K^T [causal]) V and the row LSE, on the GPU.
+
+    q, k, v: CUDA tensors of shape [B, H, N, d], contiguous, all float32 or all
+    bfloat16, on one device.  ``scale`` defaults to 1/sqrt(d).  Returns
+    ``(O, LSE)`` with O like q and LSE float32 [B, H, N] (None if
+    ``return_lse`` is False and no ``lse`` buffer was given).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must have shape [B, H, N, d], got {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError(f"q, k, v shapes differ: {tuple(q.shape)} {tuple(k.shape)} "
+                         f"{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on the same device")
+    code = _dtype_code(q.dtype)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    elif (out.shape != q.shape or out.dtype != q.dtype or out.device != q.device
+          or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32
+                              or lse.device != q.device or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None,
+                            B, H, N, d, float(scale), int(bool(causal)), code,
+                            _stream_handle(stream, q.device))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  scale: Optional[float] = None, causal: bool = False,
+                  device: Optional[torch.device] = None,
+                  stream: Optional[torch.cuda.Stream] = None,
+                  buffers: Optional[dict] = None
+                  ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """End-to-end call from host memory: copy Q, K, V to the device, run
+    attn_fwd, copy O and LSE back, all on one stream.
+
+    q, k, v: CPU tensors [B, H, N, d] (pinned memory gives asynchronous copies).
+    ``buffers`` may carry reusable device and pinned-host tensors (keys q, k, v,
+    o, lse, o_host, lse_host) so repeated calls do not allocate.  Returns CPU
+    (O, LSE); the call returns after the result is on the host.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise ValueError(f"{name} must be a CPU tensor")
+    device = torch.device(device if device is not None else "cuda")
+    bufs = buffers if buffers is not None else {}
+    B, H, N, d = q.shape
+
+    def _buf(key, like, dev, pin=False, shape=None, dtype=None):
+        t = bufs.get(key)
+        shp = tuple(shape if shape is not None else like.shape)
+        dt = dtype if dtype is not None else like.dtype
+        if t is None or tuple(t.shape) != shp or t.dtype != dt:
+            if dev.type == "cuda":
+                t = torch.empty(shp, dtype=dt, device=dev)
+            else:
+                t = torch.empty(shp, dtype=dt, pin_memory=pin)
+            bufs[key] = t
+        return t
+
+    with torch.cuda.device(device):
+        s = stream if stream is not None else torch.cuda.current_stream(device)
+        with torch.cuda.stream(s):
+            qd = _buf("q", q, device)
+            kd = _buf("k", k, device)
+            vd = _buf("v", v, device)
+            qd.copy_(q, non_blocking=True)
+            kd.copy_(k, non_blocking=True)
+            vd.copy_(v, non_blocking=True)
+            od = _buf("o", q, device)
+            ld = _buf("lse", q, device, shape=(B, H, N), dtype=torch.float32)
+            attn_fwd(qd, kd, vd, scale, causal, out=od, lse=ld, stream=s)
+            oh = _buf("o_host", q, torch.device("cpu"), pin=True)
+            lh = _buf("lse_host", q, torch.device("cpu"), pin=True, shape=(B, H, N),
+                      dtype=torch.float32)
+            oh.copy_(od, non_blocking=True)
+            lh.copy_(ld, non_blocking=True)
+        s.synchronize()
+    return oh, lh
+
+
+def row_softmax(x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                return_lse: bool = False, stream: Optional[torch.cuda.Stream] = None):
+    """Row softmax over the last dim of a contiguous float32 CUDA matrix."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("row_softmax expects a contiguous matrix")
+    if x.dtype != torch.float32:
+        raise ValueError("row_softmax expects float32")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like x")
+    lse = torch.empty(x.shape[0], dtype=torch.float32, device=x.device) if return_lse else None
+    with torch.cuda.device(x.device):
+        st = lib().attn_row_softmax(x.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None,
+                                    x.shape[0], x.shape[1], _stream_handle(stream, x.device))
+    _check(st, "attn_row_softmax")
+    return (out, lse) if return_lse else out
+
+
+def device_status(stream: Optional[torch.cuda.Stream] = None,
+                  device: Optional[torch.device] = None) -> int:
+    """Synchronise and return (and clear) the device's status word."""
+    device = torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(device):
+        return int(lib().attn_device_status(_stream_handle(stream, device)))
+
+
+def selftest_wait_timeout(timeout_ns: int = 2_000_000,
+                          device: Optional[torch.device] = None) -> int:
+    """Run the bounded-wait self test; returns the status it read back."""
+    device = torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(device):
+        return int(lib().attn_selftest_wait_timeout(int(timeout_ns),
+                                                    _stream_handle(None, device)))

@@ -1,0 +1,39 @@
+// attn_internal.h -- host-side declarations shared by the library's .cu files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/attn_fwd.h"
+
+namespace attn {
+
+// Everything a kernel launch needs besides the tensors themselves.
+struct LaunchCtx {
+    cudaStream_t stream;
+    uint32_t *status;     // device status word (bounded-wait timeouts)
+    uint64_t timeout_ns;  // limit for one barrier wait inside a kernel
+    int sm_count;
+};
+
+// bf16 path: tcgen05 tensor-core kernel (attn_fwd_tc.cu).
+attn_status launch_attn_fwd_bf16(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 int64_t BH, int64_t N, int d, float scale, bool causal,
+                                 const LaunchCtx &ctx);
+
+// fp32 path: exact CUDA-core kernel (attn_fwd_f32.cu).
+attn_status launch_attn_fwd_f32(const float *q, const float *k, const float *v, float *o,
+                                float *lse, int64_t BH, int64_t N, int d, float scale,
+                                bool causal, const LaunchCtx &ctx);
+
+// Row softmax (row_softmax.cu).
+attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t rows, int64_t width,
+                               const LaunchCtx &ctx);
+
+// Bounded-wait self test (attn_fwd_tc.cu).
+attn_status launch_wait_selftest(const LaunchCtx &ctx);
+
+// Largest N the bf16 kernel's grid can cover (query tiles on grid.y).
+constexpr int64_t kMaxNBf16 = 65535LL * 128;
+
+}  // namespace attn

@@ -1,0 +1,359 @@
+"""Throughput bench for the exact attention forward on GB300.
+
+One step = one attention forward (QK^T, online softmax, PV, epilogue: the
+whole path) over one batch of seeded synthetic inputs already resident in
+device memory.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+Metric: TFLOP/s with FLOP = 4*B*H*N^2*d (halved with the causal mask).
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (the only other place this file runs the
+oracle besides the ``cpu_baseline`` leg).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from attention_attn_fwd_05_gb300.inputs import WORKLOADS, make_workload_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "bf16_B1_H32_N16384_d128_causal"
+METRIC = "attention fwd TFLOP/s (4*B*H*N^2*d, causal halved) and % of GB300 bf16 peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SRC = {"bf16": "attention_attn_fwd_05_gb300/csrc/attn_fwd_tc.cu",
+              "f32": "attention_attn_fwd_05_gb300/csrc/attn_fwd_f32.cu"}
+KERNEL_NAME = {"bf16": "attn_fwd_bf16_tc_kernel", "f32": "attn_fwd_f32_kernel"}
+
+
+# ----------------------------------------------------------------- helpers ---
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash(dtype: str) -> str:
+    with open(os.path.join(ROOT, KERNEL_SRC[dtype]), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(dtype: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary for this kernel and
+    workload, or None when there is none or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", f"{KERNEL_NAME[dtype]}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not h or not t or h.group(1) != kernel_hash(dtype):
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"attn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        max_mhz = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max_mhz,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ------------------------------------------------------------- CPU oracle ---
+
+def sample_rows(w, n_rows: int, seed: int = 0):
+    """A deterministic spread of (bh, row) pairs covering every position range."""
+    rng = np.random.default_rng(seed)
+    BH = w.B * w.H
+    bh = rng.integers(0, BH, size=n_rows)
+    rows = np.linspace(0, w.N - 1, n_rows).round().astype(np.int64)
+    return bh.astype(np.int64), rows
+
+
+def sample_flops(w, rows) -> float:
+    visible = (rows + 1) if w.causal else np.full(rows.shape, w.N)
+    return float(4.0 * w.d * visible.sum())
+
+
+def time_oracle(w, q, k, v, budget_s: float):
+    """Time the oracle, as it stands, on a row sample sized to ~budget_s seconds."""
+    import oracle
+    cores = oracle.max_threads()
+    bh, rows = sample_rows(w, max(cores, 8), seed=1)
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, bh, rows)
+    t_cal = time.perf_counter() - t0
+    n = int(min(w.B * w.H * w.N, max(cores, len(rows) * budget_s / max(t_cal, 1e-6))))
+    bh, rows = sample_rows(w, n, seed=2)
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, bh, rows)
+    dt = time.perf_counter() - t0
+    return sample_flops(w, rows) / dt / 1e12, cores, n, dt
+
+
+# ------------------------------------------------------------------ arms ---
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    q, k, v = make_workload_inputs(w)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(w, q, k, v, min(per_step, 2.0))
+    vals, samples = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tf, cores, n, dt = time_oracle(w, q, k, v, per_step)
+        vals.append(tf)
+        samples.append((n, dt))
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wall * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{samples[-1][0]} query rows of {w.name} spread over all "
+                                   f"positions, {samples[-1][1]:.1f} s per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    io = w.io_bytes
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "dtype": w.dtype, "inputs": w.dist, "seed": w.seed,
+            "global_batch": w.B, "seq_len": w.N, "parallelism": "replicas (weak)",
+            "l2": ("inputs+outputs %.0f MB > %d MB L2, no flush" % (io / 1e6, L2_BYTES >> 20))
+            if io > 2 * L2_BYTES else "L2 flushed (256 MB write) before each timed step"}
+
+
+def run_ours(args, w):
+    from attention_attn_fwd_05_gb300 import attn_fwd, attn_fwd_host, device_status
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    q, k, v = make_workload_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    od = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = w.io_bytes <= 2 * L2_BYTES
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush \
+        else None
+
+    def step():
+        attn_fwd(qd, kd, vd, w.scale, w.causal, out=od, lse=lse, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if device_status(device=dev) != 0:
+        raise RuntimeError("device status reports a timeout during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_begin.record(stream)
+        for i in range(args.steps):
+            if flush:
+                scratch.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms = t_begin.elapsed_time(t_end)
+    step_ms = sum(kernel_ms) / len(kernel_ms) if flush else region_ms / args.steps
+    if device_status(device=dev) != 0:
+        raise RuntimeError("device status reports a timeout during the timed region")
+
+    # End to end through the public host-memory call: H2D of Q, K, V from pinned
+    # memory, the kernel, D2H of O and LSE, every step.
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    bufs = {}
+    for _ in range(2):
+        attn_fwd_host(qh, kh, vh, w.scale, w.causal, device=dev, buffers=bufs)
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        attn_fwd_host(qh, kh, vh, w.scale, w.causal, device=dev, buffers=bufs)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = od.numel() * od.element_size() + lse.numel() * 4
+
+    local_ms = torch.tensor([step_ms, e2e_s * 1e3], dtype=torch.float64)
+    if world > 1:
+        t = local_ms.to(dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        local_ms = t.cpu()
+    step_ms, e2e_ms = float(local_ms[0]), float(local_ms[1])
+    if rank != 0:
+        return
+    tflops = w.flops * world / (step_ms * 1e-3) / 1e12
+    e2e_tflops = w.flops * world / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    sustained = region_ms > 1000.0
+    if w.dtype == "bf16":
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        kernel_tflops = w.flops / (statistics.mean(kernel_ms) * 1e-3) / 1e12
+        traffic = profiled_traffic("bf16", w.name)
+        roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
+                    "unit": "TFLOP/s", "frac": kernel_tflops / peak, "traffic": traffic,
+                    "kernel": KERNEL_NAME["bf16"],
+                    "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} "
+                                   "bf16 dense (MEASURED_PEAKS.json)",
+                    "algorithmic_flops_per_launch": w.flops}
+    else:
+        kernel_tflops = w.flops / (statistics.mean(kernel_ms) * 1e-3) / 1e12
+        # fp32 FMA pipe: 152 SMs x 128 lanes x 2 FLOP x max SM clock.
+        alu_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        roofline = {"bound": "alu", "achieved": kernel_tflops, "peak": alu_peak,
+                    "unit": "TFLOP/s", "frac": kernel_tflops / alu_peak,
+                    "traffic": profiled_traffic("f32", w.name), "kernel": KERNEL_NAME["f32"],
+                    "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+                    "algorithmic_flops_per_launch": w.flops}
+    roofline["algorithmic_bytes_per_launch"] = w.io_bytes
+    roofline["hbm_gbs_algorithmic"] = w.io_bytes / (statistics.mean(kernel_ms) * 1e-3) / 1e9
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tf, cores, n, dt = time_oracle(w, q, k, v, args.cpu_budget)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} query rows of {w.name} spread over all positions "
+                         f"(row_flops = 4*d*visible keys), {dt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic", "config": config_of(w),
+        "pct_of_bf16_peak": 100.0 * tflops / world / roofline["peak"]
+        if w.dtype == "bf16" else None,
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

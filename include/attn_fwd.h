@@ -1,0 +1,127 @@
+/*
+ * attn_fwd.h -- C ABI of the GB300 (sm_103a) exact attention-forward library.
+ *
+ * The operation (page "Hardware Acceleration & Custom Kernels", section 2
+ * "FlashAttention: SRAM Tiling & Online Softmax"): for every batch b, head h
+ * and query row i,
+ *
+ *     O[b,h,i,:] = softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] ) V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp( scale * Q[b,h,i,:] . K[b,h,j,:] )
+ *
+ * with j over [0, N), or over [0, i] when `causal` is set.  The kernels walk
+ * K and V in tiles and keep a running row maximum and row sum (the online
+ * normalisation identity of the same section), so the N x N score matrix is
+ * never written to device memory.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense row-major [B, H, N, d] with d contiguous (element
+ *     (b,h,i,c) at offset ((b*H + h)*N + i)*d + c); Q, K and V share N.
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc or managed memory
+ *     on the current device), 16-byte aligned.  The caller owns them; the
+ *     library keeps no reference after the call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream: a return of ATTN_OK
+ *     means the work was validated and enqueued, not that it finished.
+ *   - Arguments are validated on the host before anything is launched; on any
+ *     error nothing is launched and the outputs are untouched.
+ *   - The first call on a device sets up per-device state (a 256-byte device
+ *     status word, kernel attributes); make it before capturing a stream into
+ *     a CUDA graph.  No call allocates device memory after that.
+ */
+#ifndef ATTN_FWD_GB300_H
+#define ATTN_FWD_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,           /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = 2,          /* B, H or N < 1, or a size overflows the kernels' index range */
+    ATTN_ERR_DTYPE = 3,          /* dtype is not an attn_dtype value */
+    ATTN_ERR_HEADDIM = 4,        /* d is not 64 or 128 */
+    ATTN_ERR_ALIGN = 5,          /* a tensor pointer is not 16-byte aligned */
+    ATTN_ERR_ARCH = 6,           /* current device is not compute capability 10.3 (sm_103) */
+    ATTN_ERR_LAUNCH = 7,         /* the kernel launch itself failed */
+    ATTN_ERR_DEVICE_TIMEOUT = 8, /* a kernel's bounded wait ran out (reported by attn_device_status) */
+    ATTN_ERR_NOT_DEVICE = 9,     /* a pointer is not device-accessible memory of the current device */
+    ATTN_ERR_CUDA = 10           /* a CUDA runtime call failed during set-up or status read-back */
+} attn_status;
+
+typedef enum attn_dtype {
+    ATTN_F32 = 0,  /* fp32 in/out; exact fp32 FMA on CUDA cores (no TF32) */
+    ATTN_BF16 = 1  /* bf16 in/out; tcgen05 tensor-core products, fp32 accumulation */
+} attn_dtype;
+
+/*
+ * attn_fwd -- O = softmax(scale * Q K^T [+ causal mask]) V and the row LSE.
+ *
+ *   q, k, v  [B,H,N,d] inputs in `dtype` (device, read only).
+ *   o        [B,H,N,d] output in `dtype` (device, fully overwritten).  Must
+ *            not overlap q, k or v.
+ *   lse      [B,H,N] fp32 output, natural-log log-sum-exp of the scaled
+ *            logits of each row (device, fully overwritten), or NULL to skip.
+ *   B, H, N  batch, heads, sequence length; each >= 1, N < 2^31 and
+ *            B*H*N*d < 2^62.
+ *   d        head dimension: 64 or 128.
+ *   scale    multiplier applied to Q.K before the softmax (1/sqrt(d) usually).
+ *   causal   0: every key is visible; non-zero: key j visible to row i iff j <= i.
+ *   dtype    an attn_dtype value.
+ *   stream   cudaStream_t (as void*).
+ *
+ * Returns ATTN_OK or the first validation / launch error.  Faults inside a
+ * kernel are never used for signalling: a kernel whose internal wait runs out
+ * records ATTN_ERR_DEVICE_TIMEOUT in the device status word and returns; read
+ * it with attn_device_status().
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                     int dtype, void *stream);
+
+/*
+ * attn_row_softmax -- row softmax of a [rows, width] fp32 matrix in one pass
+ * over the row with a running maximum and sum (page "14. Triton and kernel
+ * fusion", section "Fusion", and its exercise on rows too long for one
+ * block; the online identity of the attention page, section 2).
+ *
+ *   x     [rows, width] fp32 input (device, read only), rows contiguous.
+ *   y     [rows, width] fp32 output (device, fully overwritten), may equal x.
+ *   lse   [rows] fp32 natural-log log-sum-exp per row, or NULL.
+ *   rows, width >= 1, rows*width < 2^62.  Any width is accepted.
+ * Returns ATTN_OK or a validation / launch error (as attn_fwd).
+ */
+attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,
+                             int64_t width, void *stream);
+
+/*
+ * attn_device_status -- synchronise `stream`, then return and clear the
+ * current device's status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT if any
+ * kernel of this library gave up a bounded wait since the last read.
+ * ATTN_ERR_CUDA if synchronising or reading back failed.
+ */
+attn_status attn_device_status(void *stream);
+
+/*
+ * attn_selftest_wait_timeout -- launch one tiny kernel that waits, with the
+ * library's bounded wait, on a barrier that nothing ever signals, using a
+ * limit of `timeout_ns` nanoseconds (clamped to [1e3, 5e9]).  The kernel
+ * gives up, records the timeout and returns; this call then returns what
+ * attn_device_status() reads (ATTN_ERR_DEVICE_TIMEOUT when the error path
+ * works).  Exists to test failure detection without faulting or hanging a GPU.
+ */
+attn_status attn_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *attn_status_string(int status);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_GB300_H */

@@ -1,0 +1,105 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects invalid arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_attn_fwd_05_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "attn_fwd.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from attention_attn_fwd_05_gb300.build import build
+    build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert set(declared_functions()) == set(binding.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(L):
+    for code in range(11):
+        assert L.attn_status_string(code)
+    assert L.attn_status_string(999) == b"unknown status"
+    assert L.attn_version() == 10000
+
+
+# Fake, never-dereferenced addresses: validation must reject these calls
+# before any CUDA call is made.
+A = 0x7F0000001000
+
+
+def call(L, q=A, k=A, v=A, o=A + 0x100000, lse=None, B=1, H=1, N=128, d=64, dtype=1):
+    return L.attn_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(0.125), 0, dtype, None)
+
+
+def test_null_pointers_rejected(L):
+    assert call(L, q=None) == 1
+    assert call(L, k=None) == 1
+    assert call(L, v=None) == 1
+    assert call(L, o=None) == 1
+
+
+@pytest.mark.parametrize("B,H,N", [(0, 1, 1), (1, 0, 1), (1, 1, 0), (-1, 1, 1), (1, 1, 2 ** 31),
+                                   (2 ** 30, 2 ** 30, 2 ** 10)])
+def test_bad_shapes_rejected(L, B, H, N):
+    assert call(L, B=B, H=H, N=N) == 2
+
+
+def test_bf16_sequence_limit(L):
+    assert call(L, N=65535 * 128 + 1) == 2
+
+
+def test_f32_head_limit(L):
+    assert call(L, B=65536, H=1, N=1, dtype=0) == 2
+
+
+@pytest.mark.parametrize("dtype", [-1, 2, 7])
+def test_bad_dtype_rejected(L, dtype):
+    assert call(L, dtype=dtype) == 3
+
+
+@pytest.mark.parametrize("d", [0, 32, 96, 256, 63])
+def test_bad_head_dim_rejected(L, d):
+    assert call(L, d=d) == 4
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o", "lse"])
+def test_misaligned_rejected(L, which):
+    kw = {which: A + 8}
+    assert call(L, **kw) == 5
+
+
+def test_row_softmax_validation(L):
+    assert L.attn_row_softmax(None, A, None, 1, 1, None) == 1
+    assert L.attn_row_softmax(A, A, None, 0, 1, None) == 2
+    assert L.attn_row_softmax(A, A, None, 1, 0, None) == 2
+    assert L.attn_row_softmax(A + 2, A, None, 1, 4, None) == 5
+
+
+def test_python_wrapper_value_errors():
+    import torch
+    from attention_attn_fwd_05_gb300 import attn_fwd, row_softmax
+    x = torch.zeros(1, 1, 4, 64)
+    with pytest.raises(ValueError):
+        attn_fwd(x, x, x)  # CPU tensors
+    with pytest.raises(ValueError):
+        row_softmax(torch.zeros(3, 4))

@@ -1,0 +1,75 @@
+"""The C ABI on a GPU: pointer checks, failure detection through the bounded
+wait, and the row-softmax entry point against the oracle."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_attn_fwd_05_gb300 import (attn_fwd, binding, device_status, row_softmax,
+                                         selftest_wait_timeout)
+from attention_attn_fwd_05_gb300.inputs import make_qkv, make_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _raw(q, k, v, o, lse=None, d=64, dtype=1):
+    B, H, N, _ = q.shape
+    return binding.lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None, B, H, N, d,
+                                  ctypes.c_float(0.125), 0, dtype,
+                                  torch.cuda.current_stream().cuda_stream)
+
+
+def test_host_pointers_rejected():
+    q, k, v = make_qkv(1, 1, 128, 64, 1, "bf16")
+    qd = q.cuda()
+    out = torch.empty_like(qd)
+    assert _raw(q, qd, qd, out) == 9             # pageable host memory
+    pinned = q.pin_memory()
+    assert _raw(qd, pinned, qd, out) == 9        # pinned host memory
+    assert _raw(qd, qd, qd, out) == 0
+    torch.cuda.synchronize()
+    assert device_status() == 0
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A wait on a barrier nothing signals gives up and reports
+    ATTN_ERR_DEVICE_TIMEOUT; the status clears and later work is correct."""
+    assert selftest_wait_timeout(2_000_000) == 8
+    assert device_status() == 0
+    q, k, v = make_qkv(1, 2, 300, 128, 3, "bf16")
+    o, lse = attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, 128 ** -0.5, True)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= 2e-2
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
+
+
+@pytest.mark.parametrize("rows,width", [(1, 1), (3, 5), (64, 1000), (8, 11264), (4, 11265),
+                                        (2, 70000), (300, 4096)])
+def test_row_softmax_parity(rows, width):
+    """Row softmax (any width, including rows past 65536) against the oracle."""
+    x = make_rows(rows, width, seed=rows + width, spread=6.0)
+    y, lse = row_softmax(x.cuda(), return_lse=True)
+    torch.cuda.synchronize()
+    y_ref, lse_ref = oracle.row_softmax(x)
+    yd = y.cpu().numpy().astype(np.float64)
+    # fp32 exp and a sum over `width` terms: relative error well under 1e-5.
+    assert np.all(np.abs(yd - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-5 * max(1.0, np.abs(lse_ref).max())
+    np.testing.assert_allclose(yd.sum(axis=1), 1.0, rtol=0, atol=1e-4)
+
+
+def test_row_softmax_masked_and_in_place():
+    x = make_rows(5, 513, seed=9, spread=3.0)
+    x[:, ::7] = float("-inf")
+    y_ref, _ = oracle.row_softmax(torch.where(torch.isinf(x), torch.full_like(x, -1e30), x))
+    xd = x.cuda()
+    row_softmax(xd, out=xd)  # in place
+    torch.cuda.synchronize()
+    yd = xd.cpu().numpy().astype(np.float64)
+    assert (yd[:, ::7] == 0).all()
+    assert np.all(np.abs(yd - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)

@@ -1,0 +1,186 @@
+"""GPU parity: the CUDA library against the float64 oracle, through the C ABI.
+
+Tolerances (elementwise):
+  fp32 path:  |o - o*| <= 1e-5 * max|V| + 1e-5 * |o*|
+              |lse - lse*| <= 2e-5 + 1e-5 * |lse*|
+  bf16 path:  max |o - o*| <= 2e-2 and max |lse - lse*| <= 1e-3
+The oracle sees exactly the values the GPU sees (bf16 widened to float32).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_attn_fwd_05_gb300 import attn_fwd, device_status, inputs
+from attention_attn_fwd_05_gb300.inputs import WORKLOADS, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+F32_ATOL_V, F32_RTOL = 1e-5, 1e-5
+F32_LSE_ATOL, F32_LSE_RTOL = 2e-5, 1e-5
+BF16_O_ATOL, BF16_LSE_ATOL = 2e-2, 1e-3
+
+
+def _scale(d):
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+
+
+def assert_close(dtype, o, lse, o_ref, lse_ref, vmax, what=""):
+    o = np.asarray(o, np.float64)
+    lse = np.asarray(lse, np.float64)
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), f"{what}: non-finite output"
+    if dtype == "f32":
+        tol = F32_ATOL_V * vmax + F32_RTOL * np.abs(o_ref)
+        bad = np.abs(o - o_ref) > tol
+        assert not bad.any(), (f"{what}: {bad.sum()} O elements out of tolerance, max err "
+                               f"{np.abs(o - o_ref).max():.3e}")
+        ltol = F32_LSE_ATOL + F32_LSE_RTOL * np.abs(lse_ref)
+        lbad = np.abs(lse - lse_ref) > ltol
+        assert not lbad.any(), f"{what}: LSE max err {np.abs(lse - lse_ref).max():.3e}"
+    else:
+        eo = np.abs(o - o_ref).max()
+        el = np.abs(lse - lse_ref).max()
+        assert eo <= BF16_O_ATOL, f"{what}: O max abs err {eo:.3e}"
+        assert el <= BF16_LSE_ATOL, f"{what}: LSE max abs err {el:.3e}"
+
+
+def run_gpu(q, k, v, scale, causal):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = attn_fwd(qd, kd, vd, scale, causal)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+# --------------------------------------------------- small, full oracle ---
+
+SMALL_SHAPES = [
+    (1, 1, 1), (1, 1, 2), (1, 2, 3), (2, 1, 127), (1, 2, 128), (1, 1, 129),
+    (2, 2, 300), (1, 3, 513), (1, 1, 1000),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", SMALL_SHAPES)
+def test_parity_small(dtype, d, causal, B, H, N):
+    q, k, v = make_qkv(B, H, N, d, seed=1000 + N + d, dtype=dtype)
+    scale = _scale(d)
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    assert_close(dtype, o, lse, o_ref, lse_ref, float(v.float().abs().max()),
+                 f"{dtype} d={d} causal={causal} {B}x{H}x{N}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_parity_stress_logits_small(causal):
+    """Large logits (variance-16 Q and K) on a ragged size: online-softmax stability."""
+    q, k, v = make_qkv(1, 2, 700, 128, seed=77, dtype="bf16", dist="stress")
+    scale = _scale(128)
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    assert_close("bf16", o, lse, o_ref, lse_ref, 1.0, "stress")
+
+
+def test_lse_optional():
+    q, k, v = make_qkv(1, 1, 200, 64, seed=5, dtype="bf16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, _ = attn_fwd(qd, kd, vd, causal=True)
+    o2, lse = attn_fwd(qd, kd, vd, causal=True, return_lse=False)
+    torch.cuda.synchronize()
+    assert lse is None
+    assert torch.equal(o1, o2)
+
+
+# ------------------------------------------------ the named workloads ---
+
+def _sample_rows(w, rng):
+    """Rows checked per workload: tile edges, the ragged tail, random rows."""
+    N = w.N
+    base = {0, 1, 63, 64, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1}
+    base |= set(rng.integers(0, N, size=24).tolist())
+    return sorted(r for r in base if 0 <= r < N)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_parity_workload(name):
+    """Every named workload at full size, in the launch configuration the bench
+    times: all outputs against the oracle where it is cheap, else sampled rows
+    of every head (plus one whole last tile)."""
+    w = WORKLOADS[name]
+    q, k, v = inputs.make_workload_inputs(w)
+    o, lse = run_gpu(q, k, v, w.scale, w.causal)
+    vmax = float(v.float().abs().max())
+    if w.B * w.H * w.N * w.N * w.d <= 2 ** 33:
+        o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.scale, w.causal)
+        assert_close(w.dtype, o, lse, o_ref, lse_ref, vmax, name)
+        return
+    rng = np.random.default_rng(w.seed)
+    BH = w.B * w.H
+    rows = _sample_rows(w, rng)
+    bh_idx = np.repeat(np.arange(BH), len(rows))
+    row_idx = np.tile(np.array(rows), BH)
+    tail = np.arange(max(0, w.N - 128), w.N)  # one whole last tile of the last head
+    bh_idx = np.concatenate([bh_idx, np.full(tail.shape, BH - 1)])
+    row_idx = np.concatenate([row_idx, tail])
+    o_ref, lse_ref = oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, bh_idx, row_idx)
+    of = o.reshape(BH, w.N, w.d)[bh_idx, row_idx]
+    lf = lse.reshape(BH, w.N)[bh_idx, row_idx]
+    assert_close(w.dtype, of, lf, o_ref, lse_ref, vmax, name)
+
+
+# --------------------------------------------------- GPU invariances ---
+
+def test_t3g_key_shift_on_gpu():
+    """K' = K + 1 u^T: O unchanged, LSE shifted by scale * q.u (fp32, exact inputs)."""
+    q, k, v = make_qkv(1, 2, 300, 64, seed=31, dtype="f32")
+    u = (torch.arange(64) % 8).float() / 4 - 1  # multiples of 1/4: K + u stays exact
+    k = torch.round(k * 64) / 64
+    k2 = k + u
+    assert torch.equal(k2 - u, k)
+    scale = _scale(64)
+    o1, l1 = run_gpu(q, k, v, scale, True)
+    o2, l2 = run_gpu(q, k2, v, scale, True)
+    np.testing.assert_allclose(o2, o1, rtol=1e-4, atol=2e-5)
+    shift = (scale * (q.double() @ u.double())).numpy()
+    np.testing.assert_allclose(l2, l1 + shift, rtol=1e-5, atol=5e-5)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_t4g_permutation_on_gpu(dtype):
+    """Permuting K and V rows together (non-causal) leaves O and LSE unchanged."""
+    q, k, v = make_qkv(1, 2, 333, 128, seed=32, dtype=dtype)
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(333))
+    o1, l1 = run_gpu(q, k, v, _scale(128), False)
+    o2, l2 = run_gpu(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), _scale(128),
+                     False)
+    if dtype == "f32":
+        np.testing.assert_allclose(o2, o1, rtol=1e-4, atol=2e-5)
+        np.testing.assert_allclose(l2, l1, rtol=1e-5, atol=2e-5)
+    else:
+        assert np.abs(o2 - o1).max() <= 2 * BF16_O_ATOL
+        assert np.abs(l2 - l1).max() <= 2 * BF16_LSE_ATOL
+
+
+def test_deterministic_repeat():
+    q, k, v = make_qkv(2, 2, 1000, 128, seed=33, dtype="bf16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = attn_fwd(qd, kd, vd, causal=True)
+    o2, l2 = attn_fwd(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_non_default_stream():
+    q, k, v = make_qkv(1, 4, 777, 64, seed=34, dtype="bf16")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        o, lse = attn_fwd(qd, kd, vd, causal=False, stream=s)
+    s.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, _scale(64), False)
+    assert_close("bf16", o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, 5.0,
+                 "stream")
