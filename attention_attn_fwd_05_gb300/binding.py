@@ -25,7 +25,8 @@ STATUS_NAMES = {
     8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
 }
 EXPORTED = ("attn_fwd", "attn_row_softmax", "attn_device_status",
-            "attn_selftest_wait_timeout", "attn_status_string", "attn_version")
+            "attn_selftest_wait_timeout", "attn_last_cuda_error", "attn_status_string",
+            "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -38,7 +39,8 @@ class AttnError(RuntimeError):
         self.status = int(status)
         name = STATUS_NAMES.get(self.status, str(status))
         msg = lib().attn_status_string(self.status).decode()
-        super().__init__(f"{where}: {name} ({msg})")
+        cuda = lib().attn_last_cuda_error().decode()
+        super().__init__(f"{where}: {name} ({msg}; last CUDA error: {cuda})")
 
 
 def lib():
@@ -58,6 +60,8 @@ def lib():
         L.attn_row_softmax.argtypes = [vp, vp, vp, i64, i64, vp]
         L.attn_device_status.argtypes = [vp]
         L.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.attn_last_cuda_error.argtypes = []
+        L.attn_last_cuda_error.restype = ctypes.c_char_p
         L.attn_status_string.argtypes = [ctypes.c_int]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []

@@ -87,7 +87,16 @@ LaunchCtx make_ctx(const DeviceState &s, void *stream, uint64_t timeout_ns) {
     return LaunchCtx{static_cast<cudaStream_t>(stream), s.status, timeout_ns, s.sm_count};
 }
 
+thread_local cudaError_t t_last_error = cudaSuccess;
+
 }  // namespace
+
+attn_status check_launch(cudaError_t e, attn_status on_error) {
+    if (e == cudaSuccess) return ATTN_OK;
+    t_last_error = e;
+    return on_error;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -174,6 +183,10 @@ extern "C" const char *attn_status_string(int status) {
         case ATTN_ERR_CUDA: return "CUDA runtime call failed";
         default: return "unknown status";
     }
+}
+
+extern "C" const char *attn_last_cuda_error(void) {
+    return cudaGetErrorString(t_last_error);
 }
 
 extern "C" int attn_version(void) { return 10000; }

@@ -182,7 +182,7 @@ static attn_status launch(const float *q, const float *k, const float *v, float 
     dim3 grid((unsigned)((N + ROWS - 1) / ROWS), (unsigned)BH);
     attn_fwd_f32_kernel<D, TPR><<<grid, NUM_THREADS, 0, ctx.stream>>>(q, k, v, o, lse, (int)N,
                                                                        scale, causal ? 1 : 0);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 
 }  // namespace f32

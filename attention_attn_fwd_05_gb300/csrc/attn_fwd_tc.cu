@@ -6,20 +6,28 @@
 // m_new = max(m_old, x), d_new = d_old e^(m_old - m_new) + e^(x - m_new)
 // applied per key tile, rescaling the running output sums as tiles arrive).
 //
-// One CTA owns one 128-row query tile of one (batch, head) and walks the key
-// tiles j = 0 .. T-1 (up to the diagonal with the causal mask).  Roles:
+// One CTA owns two 128-row query tiles (A: rows r0..r0+127, B: r0+128..r0+255)
+// of one (batch, head) and walks the key tiles j = 0 .. T-1 (up to the
+// diagonal with the causal mask).  Both tiles share every K and V tile.
 //
-//   warp 4      TMA producer: Q once, then K_j and V_j into an NSTAGE-deep
-//               shared-memory ring (128-byte swizzle, 64-column boxes).
-//   warp 5      TMEM allocator and MMA issuer (one thread):
-//                 S_j  = Q K_j^T  -> TMEM buffer j%2 (128 lanes x 128 fp32 cols)
-//                 O   += P_j V_j  -> TMEM (128 lanes x d fp32 cols)
-//               S_{j+1} is issued before waiting for P_j, so the tensor core
-//               computes the next logits while the softmax warps work.
-//   warps 0-3   softmax and epilogue, one query row per thread (TMEM lane =
-//               row): read S_j, scale to log2 units, mask, running max m and
-//               sum l, P_j = 2^(s - m) as bf16 into shared memory, rescale the
-//               O row in TMEM by 2^(m_old - m_new) when the max moved; at the
+//   warp 8      TMA producer: Q_A and Q_B once, then K and V tiles into a
+//               ring of NSLOT shared-memory slots (128-byte swizzle, 64-column
+//               boxes), in the order the MMAs consume them:
+//               K_0, K_1, V_0, K_2, V_1, ...  so every load has about one full
+//               key-tile period to land.
+//   warp 9      TMEM allocator and MMA issuer (one thread).  Per key tile j:
+//                 S_A(j+1) = Q_A K_{j+1}^T,  S_B(j+1) = Q_B K_{j+1}^T
+//                 O_A += P_A(j) V_j,         O_B += P_B(j) V_j
+//               S and O accumulate in TMEM (fp32); P comes from shared memory.
+//               The next logits are computed while the softmax warps work on
+//               the current ones.
+//   warps 0-3   softmax + epilogue of tile A, one query row per thread (TMEM
+//   warps 4-7   lane = row); same for tile B.  Per key tile: read S, mask,
+//               row max (tree), p = 2^(s*scale*log2e - m) as bf16 into shared
+//               memory, row sum; the O row in TMEM is rescaled only when the
+//               row max grew by more than 2^8 since the reference it was last
+//               scaled to (the reference only has to bound the exponentials;
+//               O and l always share it, so the result is unchanged).  At the
 //               end O / l -> bf16 -> shared -> TMA store, LSE = (m + log2 l) ln 2.
 //
 // The N x N logits live only in TMEM and registers; device memory sees Q, K,
@@ -37,41 +45,46 @@ namespace tc {
 
 constexpr int BM = 128;           // query rows per tile (one per TMEM lane)
 constexpr int BN = 128;           // keys per tile
-constexpr int NUM_THREADS = 192;  // 4 softmax warps + producer warp + MMA warp
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr int NUM_THREADS = 320;  // 2 softmax warpgroups + TMA warp + MMA warp
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_S0 = 0, TMEM_S1 = 128, TMEM_O = 256;
 constexpr float LN2 = 0.69314718055994530942f;
+// Rescale O only when the running max grew by more than this (log2 units):
+// exponentials are then bounded by 2^8, far inside fp32 and bf16 range.
+constexpr float RESCALE_THRESHOLD = 8.0f;
 
 template <int D>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
-    static constexpr int NSTAGE = (D == 128) ? 2 : 4;
+    static constexpr int NSLOT = (D == 128) ? 3 : 6;
     static constexpr int DBLK = D / 64;  // 128-byte column blocks per row
     static constexpr uint32_t Q_BYTES = BM * D * 2;
-    static constexpr uint32_t KV_BYTES = BN * D * 2;
+    static constexpr uint32_t SLOT_BYTES = BN * D * 2;  // one K or V tile
     static constexpr uint32_t P_BYTES = BM * BN * 2;
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + NSTAGE * KV_BYTES;
-    static constexpr uint32_t OFF_P = OFF_V + NSTAGE * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+    static constexpr uint32_t OFF_Q = 0;                       // Q_A, Q_B
+    static constexpr uint32_t OFF_P = OFF_Q + 2 * Q_BYTES;     // P_A, P_B
+    static constexpr uint32_t OFF_KV = OFF_P + 2 * P_BYTES;    // ring
+    static constexpr uint32_t OFF_BAR = OFF_KV + NSLOT * SLOT_BYTES;
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + base alignment slack
-    // Barrier slots (8 bytes each) inside the BAR area.
+    // TMEM columns: S_A, S_B (128 fp32 columns each), O_A, O_B (D each).
+    static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+    // Barrier slots (8 bytes each).
     static constexpr int B_Q = 0;
-    static constexpr int B_KFULL = 1;
-    static constexpr int B_VFULL = B_KFULL + NSTAGE;
-    static constexpr int B_KVEMPTY = B_VFULL + NSTAGE;
-    static constexpr int B_SFULL = B_KVEMPTY + NSTAGE;  // 2
-    static constexpr int B_SFREE = B_SFULL + 2;         // 2
-    static constexpr int B_PFULL = B_SFREE + 2;
-    static constexpr int B_ODONE = B_PFULL + 1;
-    static constexpr int B_DRAIN = B_ODONE + 1;
+    static constexpr int B_FULL = 1;
+    static constexpr int B_EMPTY = B_FULL + NSLOT;
+    static constexpr int B_SFULL = B_EMPTY + NSLOT;  // [2]
+    static constexpr int B_SFREE = B_SFULL + 2;      // [2]
+    static constexpr int B_PFULL = B_SFREE + 2;      // [2]
+    static constexpr int B_ODONE = B_PFULL + 2;      // [2]
+    static constexpr int B_DRAIN = B_ODONE + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
     static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
     static_assert(8 * NUM_BARS + 8 <= BAR_BYTES, "barrier area too small");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget exceeded");
+    static_assert(TM_O1 + D <= TMEM_COLS, "TMEM budget exceeded");
 };
 
 // Wait that only honours the time limit (not the abort flag): used to drain
@@ -85,13 +98,182 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
+// Key tiles each query tile of a CTA visits: T_A <= T_B.
+__device__ __forceinline__ void tile_counts(int N, int cta_tile, int causal, int &TA, int &TB) {
+    const int nkv = (N + BN - 1) / BN;
+    if (causal) {
+        TA = min(2 * cta_tile + 1, nkv);
+        TB = min(2 * cta_tile + 2, nkv);
+    } else {
+        TA = TB = nkv;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void softmax_warpgroup(
+    int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int row0, int N, int causal,
+    float scale_log2, float *__restrict__ lse, int bh, const CUtensorMap *tmO, const WaitCtl &ctl,
+    volatile uint32_t *abort_flag) {
+    using C = Cfg<D>;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (x ? C::TM_S1 : C::TM_S0);
+    const uint32_t tO = tmem + lane_base + (x ? C::TM_O1 : C::TM_O0);
+    const uint32_t sP = sbase + C::OFF_P + x * C::P_BYTES;
+    const int tile_row0 = row0 + x * BM;
+    const int row = tile_row0 + t;
+    const int limit = causal ? min(N, row + 1) : N;  // keys [0, limit) are visible
+    const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+        ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL + x), j & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[4][32];
+        tmem_ld_32x32b_x32(tS + 0, r[0]);
+        tmem_ld_32x32b_x32(tS + 32, r[1]);
+        tmem_ld_32x32b_x32(tS + 64, r[2]);
+        tmem_ld_32x32b_x32(tS + 96, r[3]);
+        tmem_wait_ld_x32(r[0]);
+        tmem_wait_ld_x32(r[1]);
+        tmem_wait_ld_x32(r[2]);
+        tmem_wait_ld_x32(r[3]);
+        tc_fence_before();
+        mbar_arrive(bar(C::B_SFREE + x));
+
+        const int key0 = j * BN;
+        if (key0 + BN > limit) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+                if (key0 + c >= limit) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        }
+        // Row max of the raw logits (scale > 0 commutes with max): 8
+        // independent 3-input chains, then a short combine.
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i >> 1][(i & 1) * 16]);
+#pragma unroll
+        for (int c = 1; c < 16; c += 2) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int base = (i & 1) * 16;
+                mx8[i] = fmax3(mx8[i], __uint_as_float(r[i >> 1][base + c]),
+                               __uint_as_float(r[i >> 1][base + (c + 1 < 16 ? c + 1 : c)]));
+            }
+        }
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        const float m_new = mx * scale_log2;
+        const bool upd = m_new > m_ref + RESCALE_THRESHOLD;
+        float m_use = upd ? m_new : m_ref;
+        if (m_use == -INFINITY) m_use = 0.f;  // row fully masked so far (never for valid rows)
+        const float alpha = upd ? ex2_approx(m_ref - m_use) : 1.f;  // 0 on the first tile
+
+        // p = 2^(s * scale_log2 - m_use): one packed FMA per pair, one MUFU
+        // exp2 per element; four packed partial sums.
+        const uint64_t neg_m = pack_f32x2(-m_use, -m_use);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+            const uint64_t sv = pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
+                                           __uint_as_float(r[c >> 5][(c & 31) + 1]));
+            float a0, a1;
+            unpack_f32x2(ffma2(sv, scale2, neg_m), a0, a1);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pack_f32x2(p0, p1));
+            pk[c >> 1] = pack_bf16x2(p0, p1);
+        }
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        unpack_f32x2(acc[0], s0, s1);
+        unpack_f32x2(acc[1], s2, s3);
+        unpack_f32x2(acc[2], s4, s5);
+        unpack_f32x2(acc[3], s6, s7);
+        const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+
+        if (j > 0) {
+            // P_{j-1} V_{j-1} must be done: it reads the P buffer and
+            // accumulates into the O row rescaled below.
+            ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + x), (j - 1) & 1, ctl));
+            if (!ok) break;
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, upd)) {
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tO + c, o);
+                    tmem_wait_ld_x32(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_32x32b_x32(tO + c, o);
+                }
+                tmem_wait_st();
+            }
+        }
+        // P row t -> shared memory, K-major with the 128-byte swizzle the MMA
+        // descriptor expects (16-byte chunk c of row t at chunk c ^ (t & 7)).
+#pragma unroll
+        for (int c16 = 0; c16 < BN / 8; ++c16) {
+            const uint32_t addr = sP + (c16 >> 3) * (BM * 128) + t * 128 +
+                                  ((((uint32_t)c16 & 7u) ^ ((uint32_t)t & 7u)) << 4);
+            st_shared_v4(addr, pk[c16 * 4 + 0], pk[c16 * 4 + 1], pk[c16 * 4 + 2],
+                         pk[c16 * 4 + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PFULL + x));
+        l_run = l_run * alpha + rs;
+        m_ref = m_use;
+    }
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + x), (T - 1) & 1, ctl));
+    if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l_run;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO + c, o);
+            tmem_wait_ld_x32(o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int dcol = c + i * 8;
+                const uint32_t chunk = (uint32_t)(dcol & 63) >> 3;
+                const uint32_t addr = sP + (dcol >> 6) * (BM * 128) + t * 128 +
+                                      ((chunk ^ ((uint32_t)t & 7u)) << 4);
+                st_shared_v4(addr,
+                             pack_bf16x2(__uint_as_float(o[i * 8 + 0]) * inv_l,
+                                         __uint_as_float(o[i * 8 + 1]) * inv_l),
+                             pack_bf16x2(__uint_as_float(o[i * 8 + 2]) * inv_l,
+                                         __uint_as_float(o[i * 8 + 3]) * inv_l),
+                             pack_bf16x2(__uint_as_float(o[i * 8 + 4]) * inv_l,
+                                         __uint_as_float(o[i * 8 + 5]) * inv_l),
+                             pack_bf16x2(__uint_as_float(o[i * 8 + 6]) * inv_l,
+                                         __uint_as_float(o[i * 8 + 7]) * inv_l));
+            }
+        }
+        if (lse != nullptr && row < N)
+            lse[(size_t)bh * (size_t)N + (size_t)row] = (m_ref + log2f(l_run)) * LN2;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + x, BM);
+    if (t == 0 && *abort_flag == 0u && tile_row0 < N) {
+        // The tensor map clips rows >= N, so a ragged last tile is safe.
+        for (int c = 0; c < C::DBLK; ++c)
+            tma_store_3d(tmO, sP + c * (BM * 128), c * 64, tile_row0, bh);
+        tma_store_commit();
+        tma_store_wait_read();
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
                             const __grid_constant__ CUtensorMap tmO, float *__restrict__ lse,
-                            int N, int num_q_tiles, float scale_log2, int causal,
+                            int N, int num_cta_tiles, float scale_log2, int causal,
                             uint32_t *status, uint64_t timeout_ns) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -99,9 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::OFF_Q;
-    const uint32_t sK0 = sbase + C::OFF_K;
-    const uint32_t sV0 = sbase + C::OFF_V;
     const uint32_t sP = sbase + C::OFF_P;
+    const uint32_t sKV = sbase + C::OFF_KV;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM_SLOT);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_ABORT);
@@ -109,30 +290,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
-    // Heaviest causal tiles first: grid.y walks query tiles from the end.
-    const int q_tile = causal ? (num_q_tiles - 1 - (int)blockIdx.y) : (int)blockIdx.y;
-    const int row0 = q_tile * BM;
-    const int nkv = (N + BN - 1) / BN;
-    const int T = causal ? min(q_tile + 1, nkv) : nkv;  // key tiles this CTA visits
+    // Heaviest causal tiles first: grid.y walks CTA tiles from the end.
+    const int cta_tile = causal ? (num_cta_tiles - 1 - (int)blockIdx.y) : (int)blockIdx.y;
+    const int row0 = cta_tile * (2 * BM);
+    int TA, TB;
+    tile_counts(N, cta_tile, causal, TA, TB);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_Q), 1);
-        for (int s = 0; s < C::NSTAGE; ++s) {
-            mbar_init(bar(C::B_KFULL + s), 1);
-            mbar_init(bar(C::B_VFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), 1);
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(C::B_SFULL + b), 1);
-            mbar_init(bar(C::B_SFREE + b), BM);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(C::B_SFULL + x), 1);
+            mbar_init(bar(C::B_SFREE + x), BM);
+            mbar_init(bar(C::B_PFULL + x), BM);
+            mbar_init(bar(C::B_ODONE + x), 1);
         }
-        mbar_init(bar(C::B_PFULL), BM);
-        mbar_init(bar(C::B_ODONE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
@@ -142,90 +322,111 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, status, timeout_ns};
 
-    if (warp == 4) {
+    if (warp == WARP_TMA) {
         // ------------------------------------------------------ producer ---
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_Q), C::Q_BYTES);
-            for (int c = 0; c < C::DBLK; ++c)
-                tma_load_3d(sQ + c * (BM * 128), &tmQ, c * 64, row0, bh, bar(C::B_Q));
-            int j = 0;
-            for (; j < T; ++j) {
-                const int s = j % C::NSTAGE;
-                if (j >= C::NSTAGE &&
-                    !bounded_wait(bar(C::B_KVEMPTY + s), ((j / C::NSTAGE) - 1) & 1, ctl))
-                    break;
-                const uint32_t sK = sK0 + s * C::KV_BYTES, sV = sV0 + s * C::KV_BYTES;
-                mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::KV_BYTES);
+            mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::Q_BYTES);
+            for (int x = 0; x < 2; ++x)
                 for (int c = 0; c < C::DBLK; ++c)
-                    tma_load_3d(sK + c * (BN * 128), &tmK, c * 64, j * BN, bh,
-                                bar(C::B_KFULL + s));
-                mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::KV_BYTES);
+                    tma_load_3d(sQ + x * C::Q_BYTES + c * (BM * 128), &tmQ, c * 64,
+                                row0 + x * BM, bh, bar(C::B_Q));
+            // Load sequence (consumption order): K_0, then per j: K_{j+1}, V_j.
+            int n = 0;
+            bool ok = true;
+            auto load = [&](const CUtensorMap *tm, int j) -> bool {
+                const int s = n % C::NSLOT;
+                if (n >= C::NSLOT &&
+                    !bounded_wait(bar(C::B_EMPTY + s), ((n / C::NSLOT) - 1) & 1, ctl))
+                    return false;
+                const uint32_t dst = sKV + s * C::SLOT_BYTES;
+                mbar_arrive_expect_tx(bar(C::B_FULL + s), C::SLOT_BYTES);
                 for (int c = 0; c < C::DBLK; ++c)
-                    tma_load_3d(sV + c * (BN * 128), &tmV, c * 64, j * BN, bh,
-                                bar(C::B_VFULL + s));
+                    tma_load_3d(dst + c * (BN * 128), tm, c * 64, j * BN, bh, bar(C::B_FULL + s));
+                ++n;
+                return true;
+            };
+            ok = load(&tmK, 0);
+            for (int j = 0; ok && j < TB; ++j) {
+                if (j + 1 < TB && !(ok = load(&tmK, j + 1))) break;
+                ok = load(&tmV, j);
             }
-            // Let the copies issued last on each stage land before exiting
-            // (already complete on the normal path).
+            // Let the copies issued last land before exiting (already complete
+            // on the normal path).
             drain_wait(bar(C::B_Q), 0, timeout_ns);
-            for (int jj = (j > C::NSTAGE ? j - C::NSTAGE : 0); jj < j; ++jj) {
-                const int s = jj % C::NSTAGE;
-                drain_wait(bar(C::B_KFULL + s), (jj / C::NSTAGE) & 1, timeout_ns);
-                drain_wait(bar(C::B_VFULL + s), (jj / C::NSTAGE) & 1, timeout_ns);
-            }
+            for (int i = (n > C::NSLOT ? n - C::NSLOT : 0); i < n; ++i)
+                drain_wait(bar(C::B_FULL + i % C::NSLOT), (i / C::NSLOT) & 1, timeout_ns);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == WARP_MMA) {
         // ----------------------------------------------------------- MMA ---
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
-            auto issue_s = [&](int jt) {
-                const int s = jt % C::NSTAGE;
-                const uint32_t sK = sK0 + s * C::KV_BYTES;
-                const uint32_t dS = tmem + ((jt & 1) ? TMEM_S1 : TMEM_S0);
+            auto issue_s = [&](int x, uint32_t sK) {
+                const uint32_t q = sQ + x * C::Q_BYTES;
+                const uint32_t dS = tmem + (x ? C::TM_S1 : C::TM_S0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(sQ + koff, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sK + (kk >> 2) * (BN * 128) + (kk & 3) * 32,
-                                                   16, 1024);
-                    mma_bf16_ss(dS, a, b, idesc_s, kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(dS, sdesc_sw128(q + koff, 16, 1024),
+                                sdesc_sw128(sK + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(C::B_SFULL + (jt & 1)));
+                mma_commit(bar(C::B_SFULL + x));
             };
-            bool ok = bounded_wait(bar(C::B_Q), 0, ctl) &&
-                      bounded_wait(bar(C::B_KFULL + 0), 0, ctl);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-            }
-            for (int j = 0; ok && j < T; ++j) {
-                if (j + 1 < T) {
-                    const int jn = j + 1;
-                    ok = bounded_wait(bar(C::B_KFULL + jn % C::NSTAGE), (jn / C::NSTAGE) & 1, ctl);
-                    if (ok && jn >= 2)
-                        ok = bounded_wait(bar(C::B_SFREE + (jn & 1)), ((jn >> 1) - 1) & 1, ctl);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(jn);
-                }
-                const int s = j % C::NSTAGE;
-                ok = bounded_wait(bar(C::B_PFULL), j & 1, ctl) &&
-                     bounded_wait(bar(C::B_VFULL + s), (j / C::NSTAGE) & 1, ctl);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t sV = sV0 + s * C::KV_BYTES;
+            auto issue_pv = [&](int x, uint32_t sV, bool first) {
+                const uint32_t p = sP + x * C::P_BYTES;
+                const uint32_t dO = tmem + (x ? C::TM_O1 : C::TM_O0);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t a =
-                        sdesc_sw128(sP + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
-                    // V tile is MN-major (d contiguous): 16 keys = 2 swizzle atoms of
-                    // 8 rows x 128 B; the two 64-column halves sit BN*128 bytes apart.
-                    const uint64_t b = sdesc_sw128(sV + kk * (16 * 128), BN * 128, 1024);
-                    mma_bf16_ss(tmem + TMEM_O, a, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    // V is MN-major (d contiguous): 16 keys = 2 swizzle atoms of
+                    // 8 rows x 128 B; the two 64-column halves sit BN*128 B apart.
+                    mma_bf16_ss(dO, sdesc_sw128(p + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024),
+                                sdesc_sw128(sV + kk * (16 * 128), BN * 128, 1024), idesc_o,
+                                (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(C::B_ODONE));
-                mma_commit(bar(C::B_KVEMPTY + s));
+                mma_commit(bar(C::B_ODONE + x));
+            };
+            int n = 0;
+            auto acquire = [&](uint32_t &addr) -> bool {
+                const int s = n % C::NSLOT;
+                addr = sKV + s * C::SLOT_BYTES;
+                return bounded_wait(bar(C::B_FULL + s), (n / C::NSLOT) & 1, ctl);
+            };
+            auto release = [&]() {
+                mma_commit(bar(C::B_EMPTY + n % C::NSLOT));
+                ++n;
+            };
+            uint32_t sK = 0, sV = 0;
+            bool ok = bounded_wait(bar(C::B_Q), 0, ctl) && acquire(sK);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, sK);
+                issue_s(1, sK);
+                release();
+            }
+            for (int j = 0; ok && j < TB; ++j) {
+                if (j + 1 < TB) {
+                    if (!(ok = acquire(sK))) break;
+                    if (j + 1 < TA) {
+                        if (!(ok = bounded_wait(bar(C::B_SFREE + 0), j & 1, ctl))) break;
+                        tc_fence_after();
+                        issue_s(0, sK);
+                    }
+                    if (!(ok = bounded_wait(bar(C::B_SFREE + 1), j & 1, ctl))) break;
+                    tc_fence_after();
+                    issue_s(1, sK);
+                    release();
+                }
+                if (!(ok = acquire(sV))) break;
+                if (j < TA) {
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl))) break;
+                    tc_fence_after();
+                    issue_pv(0, sV, j == 0);
+                }
+                if (!(ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl))) break;
+                tc_fence_after();
+                issue_pv(1, sV, j == 0);
+                release();
             }
             // Every MMA issued above must finish before TMEM is released.
             mma_commit(bar(C::B_DRAIN));
@@ -234,137 +435,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------- softmax + epilogue ---
-        const int t = threadIdx.x;  // row within the tile == TMEM lane
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t tO = tmem + lane_base + TMEM_O;
-        const int row = row0 + t;
-        const int limit = causal ? min(N, row + 1) : N;  // keys [0, limit) are visible
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; j < T; ++j) {
-            const int b = j & 1;
-            ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL + b), (j >> 1) & 1, ctl));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t tS = tmem + lane_base + (b ? TMEM_S1 : TMEM_S0);
-            uint32_t r0[32], r1[32], r2[32], r3[32];
-            tmem_ld_32x32b_x32(tS + 0, r0);
-            tmem_ld_32x32b_x32(tS + 32, r1);
-            tmem_ld_32x32b_x32(tS + 64, r2);
-            tmem_ld_32x32b_x32(tS + 96, r3);
-            tmem_wait_ld_x32(r0);
-            tmem_wait_ld_x32(r1);
-            tmem_wait_ld_x32(r2);
-            tmem_wait_ld_x32(r3);
-            tc_fence_before();
-            mbar_arrive(bar(C::B_SFREE + b));
-
-            float s[BN];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                s[c] = __uint_as_float(r0[c]) * scale_log2;
-                s[32 + c] = __uint_as_float(r1[c]) * scale_log2;
-                s[64 + c] = __uint_as_float(r2[c]) * scale_log2;
-                s[96 + c] = __uint_as_float(r3[c]) * scale_log2;
-            }
-            const int key0 = j * BN;
-            if (key0 + BN > limit) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    if (key0 + c >= limit) s[c] = -INFINITY;
-            }
-            float mx = m_run;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
-            const float m_use = (mx == -INFINITY) ? 0.f : mx;
-            const float alpha = ex2_approx(m_run - m_use);
-            float rs = 0.f;
-            uint32_t pk[BN / 2];
-#pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                const float p0 = ex2_approx(s[c] - m_use);
-                const float p1 = ex2_approx(s[c + 1] - m_use);
-                rs += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
-            }
-
-            if (j > 0) {
-                // P_{j-1} V_{j-1} must be done: it reads the P buffer and
-                // accumulates into the O row rescaled below.
-                ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE), (j - 1) & 1, ctl));
-                if (!ok) break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha < 1.f)) {
-#pragma unroll
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld_32x32b_x32(tO + c, o);
-                        tmem_wait_ld_x32(o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st_32x32b_x32(tO + c, o);
-                    }
-                    tmem_wait_st();
-                }
-            }
-            // P row t -> shared memory, K-major with the 128-byte swizzle the
-            // MMA descriptor expects (16-byte chunk c of row t at chunk c ^ (t & 7)).
-#pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16) {
-                const uint32_t addr = sP + (c16 >> 3) * (BM * 128) + t * 128 +
-                                      ((((uint32_t)c16 & 7u) ^ ((uint32_t)t & 7u)) << 4);
-                st_shared_v4(addr, pk[c16 * 4 + 0], pk[c16 * 4 + 1], pk[c16 * 4 + 2],
-                             pk[c16 * 4 + 3]);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
-            l_run = l_run * alpha + rs;
-            m_run = mx;
-        }
-        if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE), (T - 1) & 1, ctl));
-        if (ok) {
-            tc_fence_after();
-            const float inv_l = 1.f / l_run;
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld_32x32b_x32(tO + c, o);
-                tmem_wait_ld_x32(o);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int dcol = c + i * 8;
-                    const uint32_t chunk = (uint32_t)(dcol & 63) >> 3;
-                    const uint32_t addr = sP + (dcol >> 6) * (BM * 128) + t * 128 +
-                                          ((chunk ^ ((uint32_t)t & 7u)) << 4);
-                    st_shared_v4(addr,
-                                 pack_bf16x2(__uint_as_float(o[i * 8 + 0]) * inv_l,
-                                             __uint_as_float(o[i * 8 + 1]) * inv_l),
-                                 pack_bf16x2(__uint_as_float(o[i * 8 + 2]) * inv_l,
-                                             __uint_as_float(o[i * 8 + 3]) * inv_l),
-                                 pack_bf16x2(__uint_as_float(o[i * 8 + 4]) * inv_l,
-                                             __uint_as_float(o[i * 8 + 5]) * inv_l),
-                                 pack_bf16x2(__uint_as_float(o[i * 8 + 6]) * inv_l,
-                                             __uint_as_float(o[i * 8 + 7]) * inv_l));
-                }
-            }
-            if (lse != nullptr && row < N)
-                lse[(size_t)bh * (size_t)N + (size_t)row] = (m_run + log2f(l_run)) * LN2;
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, BM);
-        if (t == 0 && *abort_flag == 0u) {
-            // The tensor map clips rows >= N, so a ragged last tile is safe.
-            for (int c = 0; c < C::DBLK; ++c)
-                tma_store_3d(&tmO, sP + c * (BM * 128), c * 64, row0, bh);
-            tma_store_commit();
-            tma_store_wait_read();
-        }
+        const int x = warp >> 2;          // 0: tile A, 1: tile B
+        const int t = threadIdx.x & 127;  // row within the tile == TMEM lane
+        softmax_warpgroup<D>(x, t, warp, tmem, sbase, x ? TB : TA, row0, N, causal, scale_log2,
+                             lse, bh, &tmO, ctl, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -430,17 +508,18 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
     if (!make_tmap(&tq, q, BH, N, D) || !make_tmap(&tk, k, BH, N, D) ||
         !make_tmap(&tv, v, BH, N, D) || !make_tmap(&to, o, BH, N, D))
         return ATTN_ERR_CUDA;
-    if (cudaFuncSetAttribute(attn_fwd_bf16_tc_kernel<D>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM_BYTES) != cudaSuccess)
+    if (check_launch(cudaFuncSetAttribute(attn_fwd_bf16_tc_kernel<D>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)C::SMEM_BYTES),
+                     ATTN_ERR_CUDA) != ATTN_OK)
         return ATTN_ERR_CUDA;
-    const int num_q_tiles = (int)((N + BM - 1) / BM);
+    const int num_cta_tiles = (int)((N + 2 * BM - 1) / (2 * BM));
     const float scale_log2 = scale * 1.44269504088896340736f;
-    dim3 grid((unsigned)BH, (unsigned)num_q_tiles);
+    dim3 grid((unsigned)BH, (unsigned)num_cta_tiles);
     attn_fwd_bf16_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
-        tq, tk, tv, to, lse, (int)N, num_q_tiles, scale_log2, causal ? 1 : 0, ctx.status,
+        tq, tk, tv, to, lse, (int)N, num_cta_tiles, scale_log2, causal ? 1 : 0, ctx.status,
         ctx.timeout_ns);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 
 }  // namespace tc
@@ -455,7 +534,7 @@ attn_status launch_attn_fwd_bf16(const void *q, const void *k, const void *v, vo
 
 attn_status launch_wait_selftest(const LaunchCtx &ctx) {
     tc::wait_selftest_kernel<<<1, 32, 0, ctx.stream>>>(ctx.status, ctx.timeout_ns);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 
 }  // namespace attn

@@ -33,6 +33,10 @@ attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t row
 // Bounded-wait self test (attn_fwd_tc.cu).
 attn_status launch_wait_selftest(const LaunchCtx &ctx);
 
+// Record `e` (if it is an error) as this thread's last CUDA error and return
+// `on_error`, else ATTN_OK.  Used right after every launch.
+attn_status check_launch(cudaError_t e, attn_status on_error);
+
 // Largest N the bf16 kernel's grid can cover (query tiles on grid.y).
 constexpr int64_t kMaxNBf16 = 65535LL * 128;
 

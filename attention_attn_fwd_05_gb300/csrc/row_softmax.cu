@@ -121,7 +121,7 @@ attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t row
     const unsigned grid = (unsigned)(rows < max_grid ? rows : max_grid);
     rsm::row_softmax_kernel<<<grid, rsm::NUM_THREADS, 0, ctx.stream>>>(x, y, lse, rows, width,
                                                                        vec4 ? 1 : 0);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 
 }  // namespace attn

@@ -157,11 +157,13 @@ def time_oracle(w, q, k, v, budget_s: float):
     """Time the oracle, as it stands, on a row sample sized to ~budget_s seconds."""
     import oracle
     cores = oracle.max_threads()
-    bh, rows = sample_rows(w, max(cores, 8), seed=1)
+    n_cal = 8 * cores
+    bh, rows = sample_rows(w, n_cal, seed=1)
+    oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, bh[:cores], rows[:cores])  # warm threads
     t0 = time.perf_counter()
     oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, bh, rows)
     t_cal = time.perf_counter() - t0
-    n = int(min(w.B * w.H * w.N, max(cores, len(rows) * budget_s / max(t_cal, 1e-6))))
+    n = int(min(w.B * w.H * w.N, max(cores, n_cal * budget_s / max(t_cal, 1e-6))))
     bh, rows = sample_rows(w, n, seed=2)
     t0 = time.perf_counter()
     oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, bh, rows)

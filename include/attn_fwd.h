@@ -114,6 +114,13 @@ attn_status attn_device_status(void *stream);
  */
 attn_status attn_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 
+/*
+ * attn_last_cuda_error -- the CUDA runtime's message for the most recent CUDA
+ * error this thread's calls into the library saw (for example why a launch was
+ * rejected), or "no error".  Static string, never NULL.
+ */
+const char *attn_last_cuda_error(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *attn_status_string(int status);
 

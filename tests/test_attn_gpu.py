@@ -58,7 +58,7 @@ def run_gpu(q, k, v, scale, causal):
 
 SMALL_SHAPES = [
     (1, 1, 1), (1, 1, 2), (1, 2, 3), (2, 1, 127), (1, 2, 128), (1, 1, 129),
-    (2, 2, 300), (1, 3, 513), (1, 1, 1000),
+    (1, 1, 256), (1, 1, 257), (1, 2, 384), (2, 2, 300), (1, 3, 513), (1, 1, 1000),
 ]
 
 
