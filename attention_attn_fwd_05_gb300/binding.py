@@ -24,7 +24,7 @@ STATUS_NAMES = {
     4: "ATTN_ERR_HEADDIM", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_ARCH", 7: "ATTN_ERR_LAUNCH",
     8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
 }
-EXPORTED = ("attn_fwd", "attn_row_softmax", "attn_device_status",
+EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_last_cuda_error", "attn_status_string",
             "attn_version")
 
@@ -57,6 +57,7 @@ def lib():
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
         L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                ctypes.c_int, ctypes.c_int, vp]
+        L.attn_fwd_noalloc.argtypes = list(L.attn_fwd.argtypes)
         L.attn_row_softmax.argtypes = [vp, vp, vp, i64, i64, vp]
         L.attn_device_status.argtypes = [vp]
         L.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -65,7 +66,7 @@ def lib():
         L.attn_status_string.argtypes = [ctypes.c_int]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
-        for name in ("attn_fwd", "attn_row_softmax", "attn_device_status",
+        for name in ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_device_status",
                      "attn_selftest_wait_timeout", "attn_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L

@@ -82,6 +82,37 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int dtype, void *stream);
 
 /*
+ * attn_fwd_noalloc -- attn_fwd for callers that must never allocate device
+ * memory: for example a server whose own allocator owns every byte of the GPU,
+ * or code running where a device allocation is forbidden or would synchronise
+ * the device.  The pages have no counterpart; this is an interface addition.
+ *
+ * Arguments, results and validation are exactly those of attn_fwd, and it
+ * runs the same kernels.  The one difference is where the kernels' scratch
+ * memory lives.  attn_fwd obtains a device status word with cudaMalloc on its
+ * first call per device.  This entry point uses a 256-byte file-scope
+ * __device__ array that the library's CUDA module carries; every GPU that
+ * loads the library holds it until the process exits.  The kernels need
+ * 4 bytes of it (the status word) whatever B, H, N and d are, so no problem
+ * size exceeds it.  No call makes a cudaMalloc, cudaFree or other allocating
+ * call.
+ *
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current.  Make that first call
+ *     before capturing a stream into a CUDA graph.
+ *   - Every call shares the one array and clears its status word (an
+ *     asynchronous memset on `stream`) before launching.  Calls that overlap
+ *     on the GPU (different streams, no ordering between them) race on it.
+ *   - A bounded-wait timeout inside the kernel ends that launch early, and its
+ *     outputs are then undefined.  The timeout is recorded only in this
+ *     array, not in the word attn_device_status reads.  Callers that need
+ *     timeouts reported should use attn_fwd.
+ */
+attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                             int causal, int dtype, void *stream);
+
+/*
  * attn_row_softmax -- row softmax of a [rows, width] fp32 matrix in one pass
  * over the row with a running maximum and sum (page "14. Triton and kernel
  * fusion", section "Fusion", and its exercise on rows too long for one
