@@ -10,25 +10,31 @@
 // of one (batch, head) and walks the key tiles j = 0 .. T-1 (up to the
 // diagonal with the causal mask).  Both tiles share every K and V tile.
 //
-//   warp 8      TMA producer: Q_A and Q_B once, then K and V tiles into a
-//               ring of NSLOT shared-memory slots (128-byte swizzle, 64-column
-//               boxes), in the order the MMAs consume them:
-//               K_0, K_1, V_0, K_2, V_1, ...  so every load has about one full
-//               key-tile period to land.
-//   warp 9      TMEM allocator and MMA issuer (one thread).  Per key tile j:
-//                 S_A(j+1) = Q_A K_{j+1}^T,  S_B(j+1) = Q_B K_{j+1}^T
-//                 O_A += P_A(j) V_j,         O_B += P_B(j) V_j
-//               S and O accumulate in TMEM (fp32); P comes from shared memory.
-//               The next logits are computed while the softmax warps work on
-//               the current ones.
+//   warp 8      TMA producer: Q_A and Q_B once, then K_0, V_0, K_1, V_1, ...
+//               into a ring of NSLOT shared-memory slots (128-byte swizzle,
+//               64-column boxes).
+//   warp 9      TMEM allocator and MMA issuer (one thread).  Per key tile j it
+//               issues, in this order,
+//                 S_A(j) = Q_A K_j^T,  O_B += P_B(j-1) V_{j-1},
+//                 S_B(j) = Q_B K_j^T,  O_A += P_A(j) V_j,
+//               so the tensor core works on one tile's products while the
+//               other tile's softmax runs.  S and O accumulate in TMEM (fp32).
+//               P (bf16) is written by the softmax threads into TMEM over the
+//               S columns it came from and is read from there by the P V MMA
+//               (A operand in TMEM): P never touches shared memory.  The next
+//               S of a tile is issued after that tile's P V in the MMA stream,
+//               and tcgen05 MMAs from one thread execute in issue order, so it
+//               overwrites P only after P V has read it.
 //   warps 0-3   softmax + epilogue of tile A, one query row per thread (TMEM
 //   warps 4-7   lane = row); same for tile B.  Per key tile: read S, mask,
-//               row max (tree), p = 2^(s*scale*log2e - m) as bf16 into shared
-//               memory, row sum; the O row in TMEM is rescaled only when the
-//               row max grew by more than 2^8 since the reference it was last
-//               scaled to (the reference only has to bound the exponentials;
-//               O and l always share it, so the result is unchanged).  At the
-//               end O / l -> bf16 -> shared -> TMA store, LSE = (m + log2 l) ln 2.
+//               row max (tree), p = 2^(s*scale*log2e - m) packed to bf16 into
+//               TMEM, row sum.  The O row is rescaled only when the row max grew
+//               by more than 2^8 since the reference it was last scaled to (the
+//               reference only has to bound the exponentials; O and l always
+//               share it, so the result is unchanged).  The S_X(j) commit also
+//               covers O_X += P_X(j-1) V_{j-1}, so O is complete when S is.  At
+//               the end O / l -> bf16 -> shared (the Q buffer of the tile, no
+//               longer read) -> TMA store, and LSE = (m + log2 l) ln 2.
 //
 // The N x N logits live only in TMEM and registers; device memory sees Q, K,
 // V read and O, LSE written.
@@ -57,26 +63,24 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 template <int D>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
-    static constexpr int NSLOT = (D == 128) ? 3 : 6;
+    static constexpr int NSLOT = (D == 128) ? 5 : 8;
     static constexpr int DBLK = D / 64;  // 128-byte column blocks per row
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t SLOT_BYTES = BN * D * 2;  // one K or V tile
-    static constexpr uint32_t P_BYTES = BM * BN * 2;
-    static constexpr uint32_t OFF_Q = 0;                       // Q_A, Q_B
-    static constexpr uint32_t OFF_P = OFF_Q + 2 * Q_BYTES;     // P_A, P_B
-    static constexpr uint32_t OFF_KV = OFF_P + 2 * P_BYTES;    // ring
+    static constexpr uint32_t OFF_Q = 0;                       // Q_A, Q_B (O staging later)
+    static constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_BYTES;    // ring
     static constexpr uint32_t OFF_BAR = OFF_KV + NSLOT * SLOT_BYTES;
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + base alignment slack
-    // TMEM columns: S_A, S_B (128 fp32 columns each), O_A, O_B (D each).
+    // TMEM columns: S_A, S_B (128 fp32 columns each; P overwrites the first 64
+    // as bf16 pairs), O_A, O_B (D each).
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
     // Barrier slots (8 bytes each).
     static constexpr int B_Q = 0;
     static constexpr int B_FULL = 1;
     static constexpr int B_EMPTY = B_FULL + NSLOT;
     static constexpr int B_SFULL = B_EMPTY + NSLOT;  // [2]
-    static constexpr int B_SFREE = B_SFULL + 2;      // [2]
-    static constexpr int B_PFULL = B_SFREE + 2;      // [2]
+    static constexpr int B_PFULL = B_SFULL + 2;      // [2]
     static constexpr int B_ODONE = B_PFULL + 2;      // [2]
     static constexpr int B_DRAIN = B_ODONE + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
@@ -119,7 +123,7 @@ __device__ __forceinline__ void softmax_warpgroup(
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x ? C::TM_S1 : C::TM_S0);
     const uint32_t tO = tmem + lane_base + (x ? C::TM_O1 : C::TM_O0);
-    const uint32_t sP = sbase + C::OFF_P + x * C::P_BYTES;
+    const uint32_t sStage = sbase + C::OFF_Q + x * C::Q_BYTES;  // Q_x, reused for O
     const int tile_row0 = row0 + x * BM;
     const int row = tile_row0 + t;
     const int limit = causal ? min(N, row + 1) : N;  // keys [0, limit) are visible
@@ -139,8 +143,6 @@ __device__ __forceinline__ void softmax_warpgroup(
         tmem_wait_ld_x32(r[1]);
         tmem_wait_ld_x32(r[2]);
         tmem_wait_ld_x32(r[3]);
-        tc_fence_before();
-        mbar_arrive(bar(C::B_SFREE + x));
 
         const int key0 = j * BN;
         if (key0 + BN > limit) {
@@ -171,10 +173,11 @@ __device__ __forceinline__ void softmax_warpgroup(
         const float alpha = upd ? ex2_approx(m_ref - m_use) : 1.f;  // 0 on the first tile
 
         // p = 2^(s * scale_log2 - m_use): one packed FMA per pair, one MUFU
-        // exp2 per element; four packed partial sums.
+        // exp2 per element; four packed partial sums.  The packed bf16 pairs
+        // are written back over the first 64 S columns (P in TMEM).
         const uint64_t neg_m = pack_f32x2(-m_use, -m_use);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[BN / 2];
+        uint32_t pk[2][32];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
             const uint64_t sv = pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
@@ -183,8 +186,10 @@ __device__ __forceinline__ void softmax_warpgroup(
             unpack_f32x2(ffma2(sv, scale2, neg_m), a0, a1);
             const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
             acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pack_f32x2(p0, p1));
-            pk[c >> 1] = pack_bf16x2(p0, p1);
+            pk[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
         }
+        tmem_st_32x32b_x32(tS + 0, pk[0]);
+        tmem_st_32x32b_x32(tS + 32, pk[1]);
         float s0, s1, s2, s3, s4, s5, s6, s7;
         unpack_f32x2(acc[0], s0, s1);
         unpack_f32x2(acc[1], s2, s3);
@@ -192,43 +197,30 @@ __device__ __forceinline__ void softmax_warpgroup(
         unpack_f32x2(acc[3], s6, s7);
         const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
 
-        if (j > 0) {
-            // P_{j-1} V_{j-1} must be done: it reads the P buffer and
-            // accumulates into the O row rescaled below.
-            ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + x), (j - 1) & 1, ctl));
-            if (!ok) break;
-            tc_fence_after();
-            if (__any_sync(0xffffffffu, upd)) {
+        // O_X += P_X(j-1) V_{j-1} completed before S_X(j) did (same commit),
+        // so the O row can be rescaled here without another wait.
+        if (j > 0 && __any_sync(0xffffffffu, upd)) {
 #pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld_32x32b_x32(tO + c, o);
-                    tmem_wait_ld_x32(o);
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tO + c, o);
+                tmem_wait_ld_x32(o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st_32x32b_x32(tO + c, o);
-                }
-                tmem_wait_st();
+                for (int i = 0; i < 32; ++i)
+                    o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st_32x32b_x32(tO + c, o);
             }
         }
-        // P row t -> shared memory, K-major with the 128-byte swizzle the MMA
-        // descriptor expects (16-byte chunk c of row t at chunk c ^ (t & 7)).
-#pragma unroll
-        for (int c16 = 0; c16 < BN / 8; ++c16) {
-            const uint32_t addr = sP + (c16 >> 3) * (BM * 128) + t * 128 +
-                                  ((((uint32_t)c16 & 7u) ^ ((uint32_t)t & 7u)) << 4);
-            st_shared_v4(addr, pk[c16 * 4 + 0], pk[c16 * 4 + 1], pk[c16 * 4 + 2],
-                         pk[c16 * 4 + 3]);
-        }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + x));
         l_run = l_run * alpha + rs;
         m_ref = m_use;
     }
-    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + x), (T - 1) & 1, ctl));
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + x), 0, ctl));
     if (ok) {
+        // Q_x is no longer read: its last S MMA completed before this tile's
+        // last S was observed.  Stage O there in the O tensor map's swizzle.
         tc_fence_after();
         const float inv_l = 1.f / l_run;
 #pragma unroll
@@ -240,7 +232,7 @@ __device__ __forceinline__ void softmax_warpgroup(
             for (int i = 0; i < 4; ++i) {
                 const int dcol = c + i * 8;
                 const uint32_t chunk = (uint32_t)(dcol & 63) >> 3;
-                const uint32_t addr = sP + (dcol >> 6) * (BM * 128) + t * 128 +
+                const uint32_t addr = sStage + (dcol >> 6) * (BM * 128) + t * 128 +
                                       ((chunk ^ ((uint32_t)t & 7u)) << 4);
                 st_shared_v4(addr,
                              pack_bf16x2(__uint_as_float(o[i * 8 + 0]) * inv_l,
@@ -261,7 +253,7 @@ __device__ __forceinline__ void softmax_warpgroup(
     if (t == 0 && *abort_flag == 0u && tile_row0 < N) {
         // The tensor map clips rows >= N, so a ragged last tile is safe.
         for (int c = 0; c < C::DBLK; ++c)
-            tma_store_3d(tmO, sP + c * (BM * 128), c * 64, tile_row0, bh);
+            tma_store_3d(tmO, sStage + c * (BM * 128), c * 64, tile_row0, bh);
         tma_store_commit();
         tma_store_wait_read();
     }
@@ -281,7 +273,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::OFF_Q;
-    const uint32_t sP = sbase + C::OFF_P;
     const uint32_t sKV = sbase + C::OFF_KV;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM_SLOT);
@@ -304,7 +295,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(C::B_SFULL + x), 1);
-            mbar_init(bar(C::B_SFREE + x), BM);
             mbar_init(bar(C::B_PFULL + x), BM);
             mbar_init(bar(C::B_ODONE + x), 1);
         }
@@ -330,25 +320,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int c = 0; c < C::DBLK; ++c)
                     tma_load_3d(sQ + x * C::Q_BYTES + c * (BM * 128), &tmQ, c * 64,
                                 row0 + x * BM, bh, bar(C::B_Q));
-            // Load sequence (consumption order): K_0, then per j: K_{j+1}, V_j.
+            // Load sequence K_0, V_0, K_1, V_1, ...: load n goes to slot n % NSLOT.
             int n = 0;
-            bool ok = true;
-            auto load = [&](const CUtensorMap *tm, int j) -> bool {
+            for (; n < 2 * TB; ++n) {
                 const int s = n % C::NSLOT;
                 if (n >= C::NSLOT &&
                     !bounded_wait(bar(C::B_EMPTY + s), ((n / C::NSLOT) - 1) & 1, ctl))
-                    return false;
+                    break;
                 const uint32_t dst = sKV + s * C::SLOT_BYTES;
+                const CUtensorMap *tm = (n & 1) ? &tmV : &tmK;
                 mbar_arrive_expect_tx(bar(C::B_FULL + s), C::SLOT_BYTES);
                 for (int c = 0; c < C::DBLK; ++c)
-                    tma_load_3d(dst + c * (BN * 128), tm, c * 64, j * BN, bh, bar(C::B_FULL + s));
-                ++n;
-                return true;
-            };
-            ok = load(&tmK, 0);
-            for (int j = 0; ok && j < TB; ++j) {
-                if (j + 1 < TB && !(ok = load(&tmK, j + 1))) break;
-                ok = load(&tmV, j);
+                    tma_load_3d(dst + c * (BN * 128), tm, c * 64, (n >> 1) * BN, bh,
+                                bar(C::B_FULL + s));
             }
             // Let the copies issued last land before exiting (already complete
             // on the normal path).
@@ -362,6 +346,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
+            // Slot and phase of load n (K_j is load 2j, V_j is load 2j+1).
+            auto slot_addr = [&](int n) -> uint32_t { return sKV + (n % C::NSLOT) * C::SLOT_BYTES; };
+            auto wait_full = [&](int n) -> bool {
+                return bounded_wait(bar(C::B_FULL + n % C::NSLOT), (n / C::NSLOT) & 1, ctl);
+            };
+            auto release = [&](int n) { mma_commit(bar(C::B_EMPTY + n % C::NSLOT)); };
             auto issue_s = [&](int x, uint32_t sK) {
                 const uint32_t q = sQ + x * C::Q_BYTES;
                 const uint32_t dS = tmem + (x ? C::TM_S1 : C::TM_S0);
@@ -374,59 +364,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mma_commit(bar(C::B_SFULL + x));
             };
             auto issue_pv = [&](int x, uint32_t sV, bool first) {
-                const uint32_t p = sP + x * C::P_BYTES;
+                const uint32_t aP = tmem + (x ? C::TM_S1 : C::TM_S0);
                 const uint32_t dO = tmem + (x ? C::TM_O1 : C::TM_O0);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    // V is MN-major (d contiguous): 16 keys = 2 swizzle atoms of
-                    // 8 rows x 128 B; the two 64-column halves sit BN*128 B apart.
-                    mma_bf16_ss(dO, sdesc_sw128(p + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024),
-                                sdesc_sw128(sV + kk * (16 * 128), BN * 128, 1024), idesc_o,
-                                (!first || kk > 0) ? 1u : 0u);
+                    // P: 16 keys of bf16 pairs = 8 TMEM columns per step.  V is
+                    // MN-major (d contiguous): 16 keys = 2 swizzle atoms of 8 rows
+                    // x 128 B; the two 64-column halves sit BN*128 B apart.
+                    mma_bf16_ts(dO, aP + kk * 8, sdesc_sw128(sV + kk * (16 * 128), BN * 128, 1024),
+                                idesc_o, (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(C::B_ODONE + x));
             };
-            int n = 0;
-            auto acquire = [&](uint32_t &addr) -> bool {
-                const int s = n % C::NSLOT;
-                addr = sKV + s * C::SLOT_BYTES;
-                return bounded_wait(bar(C::B_FULL + s), (n / C::NSLOT) & 1, ctl);
-            };
-            auto release = [&]() {
-                mma_commit(bar(C::B_EMPTY + n % C::NSLOT));
-                ++n;
-            };
-            uint32_t sK = 0, sV = 0;
-            bool ok = bounded_wait(bar(C::B_Q), 0, ctl) && acquire(sK);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, sK);
-                issue_s(1, sK);
-                release();
-            }
+            bool ok = bounded_wait(bar(C::B_Q), 0, ctl);
             for (int j = 0; ok && j < TB; ++j) {
-                if (j + 1 < TB) {
-                    if (!(ok = acquire(sK))) break;
-                    if (j + 1 < TA) {
-                        if (!(ok = bounded_wait(bar(C::B_SFREE + 0), j & 1, ctl))) break;
-                        tc_fence_after();
-                        issue_s(0, sK);
-                    }
-                    if (!(ok = bounded_wait(bar(C::B_SFREE + 1), j & 1, ctl))) break;
-                    tc_fence_after();
-                    issue_s(1, sK);
-                    release();
-                }
-                if (!(ok = acquire(sV))) break;
-                if (j < TA) {
-                    if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl))) break;
-                    tc_fence_after();
-                    issue_pv(0, sV, j == 0);
-                }
-                if (!(ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl))) break;
+                const int nK = 2 * j;
+                if (!(ok = wait_full(nK))) break;
                 tc_fence_after();
-                issue_pv(1, sV, j == 0);
-                release();
+                if (j < TA) issue_s(0, slot_addr(nK));
+                if (j >= 1) {
+                    // O_B += P_B(j-1) V_{j-1}; V_{j-1} is released after it.
+                    const int nV = 2 * (j - 1) + 1;
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl) &&
+                               wait_full(nV)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(1, slot_addr(nV), j == 1);
+                    release(nV);
+                }
+                issue_s(1, slot_addr(nK));
+                release(nK);
+                if (j < TA) {
+                    const int nV = 2 * j + 1;
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl) && wait_full(nV)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(0, slot_addr(nV), j == 0);
+                    if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
+                }
+            }
+            if (ok) {
+                const int j = TB - 1, nV = 2 * j + 1;
+                ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl) && wait_full(nV);
+                if (ok) {
+                    tc_fence_after();
+                    issue_pv(1, slot_addr(nV), j == 0);
+                    release(nV);
+                    mma_commit(bar(C::B_ODONE + 1));
+                }
             }
             // Every MMA issued above must finish before TMEM is released.
             mma_commit(bar(C::B_DRAIN));

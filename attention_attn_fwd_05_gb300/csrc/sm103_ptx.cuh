@@ -71,14 +71,17 @@ enum : uint32_t {
 
 // Wait for the phase with parity `parity` of barrier `bar` to complete.
 // Returns true when it did; false if the wait ran out of time (the timeout is
-// recorded) or another thread of the CTA already gave up.
+// recorded) or another thread of the CTA already gave up.  The spin touches
+// only the barrier; the abort flag, the status word and the clock are looked
+// at every 64 polls, so waiting threads take little shared-memory bandwidth
+// from the tensor core's operand reads.
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*ctl.abort) return false;
         if ((n & 63u) == 0u) {
+            if (*ctl.abort) return false;
             // A timeout recorded by any CTA (this launch or an earlier one whose
             // status has not been read yet) makes every later wait give up at
             // once, so a broken launch winds down in one time limit, not one
@@ -95,6 +98,15 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
             }
         }
     }
+}
+
+// The same wait for a whole warp: lane 0 polls, the others wait at the
+// shuffle, and every lane gets lane 0's answer.  Call from all 32 lanes.
+__device__ __forceinline__ bool bounded_wait_warp(uint32_t bar, uint32_t parity,
+                                                  const WaitCtl &ctl) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, ctl);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // ------------------------------------------------------------------ TMA ---
