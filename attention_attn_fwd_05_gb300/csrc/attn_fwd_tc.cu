@@ -352,28 +352,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 return bounded_wait(bar(C::B_FULL + n % C::NSLOT), (n / C::NSLOT) & 1, ctl);
             };
             auto release = [&](int n) { mma_commit(bar(C::B_EMPTY + n % C::NSLOT)); };
+            // Descriptor bases; each GEMM adds fixed per-step offsets inside
+            // one asm block, so the issue loop does no descriptor arithmetic.
+            const uint64_t qdesc[2] = {sdesc_sw128(sQ, 16, 1024),
+                                       sdesc_sw128(sQ + C::Q_BYTES, 16, 1024)};
             auto issue_s = [&](int x, uint32_t sK) {
-                const uint32_t q = sQ + x * C::Q_BYTES;
                 const uint32_t dS = tmem + (x ? C::TM_S1 : C::TM_S0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    mma_bf16_ss(dS, sdesc_sw128(q + koff, 16, 1024),
-                                sdesc_sw128(sK + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-                }
+                if constexpr (D == 128)
+                    gemm_ss_k8(dS, qdesc[x], sdesc_sw128(sK, 16, 1024), idesc_s, 0u);
+                else
+                    gemm_ss_k4(dS, qdesc[x], sdesc_sw128(sK, 16, 1024), idesc_s, 0u);
                 mma_commit(bar(C::B_SFULL + x));
             };
             auto issue_pv = [&](int x, uint32_t sV, bool first) {
-                const uint32_t aP = tmem + (x ? C::TM_S1 : C::TM_S0);
-                const uint32_t dO = tmem + (x ? C::TM_O1 : C::TM_O0);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // P: 16 keys of bf16 pairs = 8 TMEM columns per step.  V is
-                    // MN-major (d contiguous): 16 keys = 2 swizzle atoms of 8 rows
-                    // x 128 B; the two 64-column halves sit BN*128 B apart.
-                    mma_bf16_ts(dO, aP + kk * 8, sdesc_sw128(sV + kk * (16 * 128), BN * 128, 1024),
-                                idesc_o, (!first || kk > 0) ? 1u : 0u);
-                }
+                // P: 16 keys of bf16 pairs = 8 TMEM columns per step.  V is
+                // MN-major (d contiguous): 16 keys = 2 swizzle atoms of 8 rows
+                // x 128 B; the two 64-column halves sit BN*128 B apart.
+                gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + (x ? C::TM_S1 : C::TM_S0),
+                           sdesc_sw128(sV, BN * 128, 1024), idesc_o, first ? 0u : 1u);
             };
             bool ok = bounded_wait(bar(C::B_Q), 0, ctl);
             for (int j = 0; ok && j < TB; ++j) {

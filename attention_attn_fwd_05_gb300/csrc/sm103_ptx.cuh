@@ -69,14 +69,10 @@ enum : uint32_t {
     STATUS_TIMEOUT = 1u << 0,
 };
 
-// Wait for the phase with parity `parity` of barrier `bar` to complete.
-// Returns true when it did; false if the wait ran out of time (the timeout is
-// recorded) or another thread of the CTA already gave up.  The spin touches
-// only the barrier; the abort flag, the status word and the clock are looked
-// at every 64 polls, so waiting threads take little shared-memory bandwidth
-// from the tensor core's operand reads.
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of bounded_wait (kept out of line so the fast path stays a
+// single try_wait): keep polling; every 64 polls look at the abort flag, the
+// status word and the clock.
+__device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl ctl) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -98,6 +94,15 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
             }
         }
     }
+}
+
+// Wait for the phase with parity `parity` of barrier `bar` to complete.
+// Returns true when it did; false if the wait ran out of time (the timeout is
+// recorded) or another thread of the CTA already gave up.  A phase that is
+// already complete costs one try_wait.
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return bounded_wait_slow(bar, parity, ctl);
 }
 
 // The same wait for a whole warp: lane 0 polls, the others wait at the
@@ -207,6 +212,59 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// One 128 x N x (16*KSTEPS) GEMM as KSTEPS back-to-back tcgen05.mma (kind::f16)
+// from shared-memory descriptors.  Step k uses a_desc + a_off[k] and
+// b_desc + b_off[k] (16-byte units added to the start-address field).  The
+// first step overwrites D unless `accumulate`; later steps accumulate.
+#define ATTN_MMA_SS_STEP(K, AOFF, BOFF)                                               \
+    "add.s64 a, %1, " #AOFF ";\n\tadd.s64 b, %2, " #BOFF ";\n\t"                        \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, " K ";\n\t"
+__device__ __forceinline__ void gemm_ss_k8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    // K-major 128-byte-swizzled operands: steps 0-3 walk 32 B within the first
+    // 64-column block, steps 4-7 the same in the block 16 KB further on.
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+        ATTN_MMA_SS_STEP("pt", 2, 2) ATTN_MMA_SS_STEP("pt", 4, 4) ATTN_MMA_SS_STEP("pt", 6, 6)
+        ATTN_MMA_SS_STEP("pt", 1024, 1024) ATTN_MMA_SS_STEP("pt", 1026, 1026)
+        ATTN_MMA_SS_STEP("pt", 1028, 1028) ATTN_MMA_SS_STEP("pt", 1030, 1030)
+        "}\n" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void gemm_ss_k4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+        ATTN_MMA_SS_STEP("pt", 2, 2) ATTN_MMA_SS_STEP("pt", 4, 4) ATTN_MMA_SS_STEP("pt", 6, 6)
+        "}\n" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+#undef ATTN_MMA_SS_STEP
+
+// 128 x N x 128 GEMM with A in TMEM (bf16 pairs, 8 columns per 16-wide step)
+// and B an MN-major shared-memory operand advancing 2048 B (16 rows of 128 B)
+// per step.
+#define ATTN_MMA_TS_STEP(ACOL, BOFF)                                                  \
+    "add.u32 ta, %1, " #ACOL ";\n\tadd.s64 b, %2, " #BOFF ";\n\t"                       \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, pt;\n\t"
+__device__ __forceinline__ void gemm_ts_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
+        "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+        ATTN_MMA_TS_STEP(8, 128) ATTN_MMA_TS_STEP(16, 256) ATTN_MMA_TS_STEP(24, 384)
+        ATTN_MMA_TS_STEP(32, 512) ATTN_MMA_TS_STEP(40, 640) ATTN_MMA_TS_STEP(48, 768)
+        ATTN_MMA_TS_STEP(56, 896)
+        "}\n" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+#undef ATTN_MMA_TS_STEP
 
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
