@@ -12,7 +12,8 @@
 //
 //   warp 8      TMA producer: Q_A and Q_B once, then K_0, V_0, K_1, V_1, ...
 //               into a ring of NSLOT shared-memory slots (128-byte swizzle,
-//               64-column boxes).
+//               64-column boxes).  Slots come back when tile B's softmax sees
+//               S_B(j) complete (see softmax_warpgroup).
 //   warp 9      TMEM allocator and MMA issuer (one thread).  Per key tile j it
 //               issues, in this order,
 //                 S_A(j) = Q_A K_j^T,  O_B += P_B(j-1) V_{j-1},
@@ -133,6 +134,14 @@ __device__ __forceinline__ void softmax_warpgroup(
     for (int j = 0; j < T; ++j) {
         ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL + x), j & 1, ctl));
         if (!ok) break;
+        if (x == 1 && t == 0) {
+            // S_B(j) is complete, and with it every MMA issued before it: S_A(j)
+            // (the last reader of K_j) and O_B += P_B(j-1) V_{j-1} (the last
+            // reader of V_{j-1}).  Hand both slots back to the producer here,
+            // which keeps two commits per key tile off the MMA issuer.
+            mbar_arrive(bar(C::B_EMPTY + (2 * j) % C::NSLOT));
+            if (j >= 1) mbar_arrive(bar(C::B_EMPTY + (2 * j - 1) % C::NSLOT));
+        }
         tc_fence_after();
         uint32_t r[4][32];
         tmem_ld_32x32b_x32(tS + 0, r[0]);
@@ -351,7 +360,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             auto wait_full = [&](int n) -> bool {
                 return bounded_wait(bar(C::B_FULL + n % C::NSLOT), (n / C::NSLOT) & 1, ctl);
             };
-            auto release = [&](int n) { mma_commit(bar(C::B_EMPTY + n % C::NSLOT)); };
             // Descriptor bases; each GEMM adds fixed per-step offsets inside
             // one asm block, so the issue loop does no descriptor arithmetic.
             const uint64_t qdesc[2] = {sdesc_sw128(sQ, 16, 1024),
@@ -375,20 +383,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int j = 0; ok && j < TB; ++j) {
                 const int nK = 2 * j;
                 if (!(ok = wait_full(nK))) break;
-                tc_fence_after();
                 if (j < TA) issue_s(0, slot_addr(nK));
                 if (j >= 1) {
-                    // O_B += P_B(j-1) V_{j-1}; V_{j-1} is released after it.
+                    // O_B += P_B(j-1) V_{j-1}.
                     const int nV = 2 * (j - 1) + 1;
                     if (!(ok = bounded_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl) &&
                                wait_full(nV)))
                         break;
                     tc_fence_after();
                     issue_pv(1, slot_addr(nV), j == 1);
-                    release(nV);
                 }
                 issue_s(1, slot_addr(nK));
-                release(nK);
                 if (j < TA) {
                     const int nV = 2 * j + 1;
                     if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl) && wait_full(nV)))
@@ -404,7 +409,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (ok) {
                     tc_fence_after();
                     issue_pv(1, slot_addr(nV), j == 0);
-                    release(nV);
                     mma_commit(bar(C::B_ODONE + 1));
                 }
             }
