@@ -24,7 +24,7 @@ STATUS_NAMES = {
     4: "ATTN_ERR_HEADDIM", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_ARCH", 7: "ATTN_ERR_LAUNCH",
     8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
 }
-EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_device_status",
+EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_add_rmsnorm", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_last_cuda_error", "attn_status_string",
             "attn_version")
 
@@ -59,6 +59,8 @@ def lib():
                                ctypes.c_int, ctypes.c_int, vp]
         L.attn_fwd_noalloc.argtypes = list(L.attn_fwd.argtypes)
         L.attn_row_softmax.argtypes = [vp, vp, vp, i64, i64, vp]
+        L.attn_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_float,
+                                       ctypes.c_int, vp]
         L.attn_device_status.argtypes = [vp]
         L.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         L.attn_last_cuda_error.argtypes = []
@@ -66,7 +68,8 @@ def lib():
         L.attn_status_string.argtypes = [ctypes.c_int]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
-        for name in ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_device_status",
+        for name in ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_add_rmsnorm",
+                     "attn_device_status",
                      "attn_selftest_wait_timeout", "attn_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -216,6 +219,39 @@ def row_softmax(x: torch.Tensor, out: Optional[torch.Tensor] = None,
     return (out, lse) if return_lse else out
 
 
+def add_rmsnorm(x: torch.Tensor, weight: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                eps: float = 1e-6, out: Optional[torch.Tensor] = None,
+                res_out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None):
+    """RMSNorm(x [+ residual]) * weight over the last dim of a contiguous matrix.
+
+    Returns ``out`` or, with a residual, ``(out, x + residual)``.
+    """
+    for name, t in (("x", x), ("weight", weight)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if x.dim() != 2:
+        raise ValueError("add_rmsnorm expects a [rows, width] matrix")
+    code = _dtype_code(x.dtype)
+    if weight.dtype != x.dtype or weight.shape != (x.shape[1],):
+        raise ValueError("weight must be a [width] tensor of x's dtype")
+    if residual is not None and (residual.shape != x.shape or residual.dtype != x.dtype
+                                 or not residual.is_contiguous() or not residual.is_cuda):
+        raise ValueError("residual must be a contiguous CUDA tensor like x")
+    out = torch.empty_like(x) if out is None else out
+    if residual is not None and res_out is None:
+        res_out = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        st = lib().attn_add_rmsnorm(x.data_ptr(),
+                                    residual.data_ptr() if residual is not None else None,
+                                    weight.data_ptr(), out.data_ptr(),
+                                    res_out.data_ptr() if residual is not None else None,
+                                    x.shape[0], x.shape[1], float(eps), code,
+                                    _stream_handle(stream, x.device))
+    _check(st, "attn_add_rmsnorm")
+    return (out, res_out) if residual is not None else out
+
+
 def device_status(stream: Optional[torch.cuda.Stream] = None,
                   device: Optional[torch.device] = None) -> int:
     """Synchronise and return (and clear) the device's status word."""
@@ -231,3 +267,49 @@ def selftest_wait_timeout(timeout_ns: int = 2_000_000,
     with torch.cuda.device(device):
         return int(lib().attn_selftest_wait_timeout(int(timeout_ns),
                                                     _stream_handle(None, device)))
+
+
+class AttnGraph:
+    """One or more attn_fwd launches captured into a CUDA graph and replayed.
+
+    The attention page's section 4 ("Compilation & Graph Capture") names the
+    cost this removes: per-launch CPU dispatch, which dominates small shapes.
+    Capture records the library's kernel launch (its argument checks and
+    tensor-map encoding run once, at capture); each replay is one driver call.
+
+    Usage: build it on static device tensors, then overwrite those tensors in
+    place and call ``replay()``.  ``calls`` is a list of (q, k, v, causal) on
+    one device; each gets its own output and LSE buffer (``outputs[i]``).
+    """
+
+    def __init__(self, calls, scale: Optional[float] = None):
+        if not calls:
+            raise ValueError("AttnGraph needs at least one call")
+        self.device = calls[0][0].device
+        self.outputs = []
+        for q, k, v, causal in calls:
+            B, H, N, _ = q.shape
+            self.outputs.append((torch.empty_like(q),
+                                 torch.empty((B, H, N), dtype=torch.float32, device=q.device)))
+        self._calls = list(calls)
+        self._scale = scale
+        # One eager pass first: per-device library set-up (status word, kernel
+        # attributes) must not happen inside the capture.
+        self._launch(torch.cuda.current_stream(self.device))
+        torch.cuda.synchronize(self.device)
+        self.graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.device(self.device), torch.cuda.stream(side):
+            with torch.cuda.graph(self.graph, stream=side):
+                self._launch(side)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+
+    def _launch(self, stream):
+        for (q, k, v, causal), (o, lse) in zip(self._calls, self.outputs):
+            attn_fwd(q, k, v, self._scale, causal, out=o, lse=lse, stream=stream)
+
+    def replay(self):
+        """Run every captured launch again on the current contents of the inputs."""
+        self.graph.replay()
+        return self.outputs

@@ -143,6 +143,28 @@ extern "C" attn_status attn_row_softmax(const float *x, float *y, float *lse, in
     return launch_row_softmax(x, y, lse, rows, width, make_ctx(*s, stream, kDefaultTimeoutNs));
 }
 
+extern "C" attn_status attn_add_rmsnorm(const void *x, const void *residual, const void *weight,
+                                        void *out, void *res_out, int64_t rows, int64_t width,
+                                        float eps, int dtype, void *stream) {
+    if (!x || !weight || !out || (residual && !res_out)) return ATTN_ERR_NULL;
+    if (rows < 1 || width < 1 || width > INT32_MAX || !product_fits(rows, width, 1, 1))
+        return ATTN_ERR_SHAPE;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+    if (!aligned16(x) || !aligned16(residual) || !aligned16(weight) || !aligned16(out) ||
+        !aligned16(res_out))
+        return ATTN_ERR_ALIGN;
+    DeviceState *s = nullptr;
+    attn_status st = device_state(&s);
+    if (st != ATTN_OK) return st;
+    for (const void *p : {x, weight, static_cast<const void *>(out)})
+        if ((st = check_device_ptr(p)) != ATTN_OK) return st;
+    if (residual && ((st = check_device_ptr(residual)) != ATTN_OK ||
+                     (st = check_device_ptr(res_out)) != ATTN_OK))
+        return st;
+    return launch_add_rmsnorm(x, residual, weight, out, residual ? res_out : nullptr, rows, width,
+                              eps, dtype, make_ctx(*s, stream, kDefaultTimeoutNs));
+}
+
 extern "C" attn_status attn_device_status(void *stream) {
     DeviceState *s = nullptr;
     attn_status st = device_state(&s);

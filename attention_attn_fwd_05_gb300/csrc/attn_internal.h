@@ -30,6 +30,11 @@ attn_status launch_attn_fwd_f32(const float *q, const float *k, const float *v, 
 attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t rows, int64_t width,
                                const LaunchCtx &ctx);
 
+// Residual add + RMSNorm (add_rmsnorm.cu).
+attn_status launch_add_rmsnorm(const void *x, const void *residual, const void *weight, void *out,
+                               void *res_out, int64_t rows, int64_t width, float eps, int dtype,
+                               const LaunchCtx &ctx);
+
 // Bounded-wait self test (attn_fwd_tc.cu).
 attn_status launch_wait_selftest(const LaunchCtx &ctx);
 

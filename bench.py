@@ -339,6 +339,68 @@ def run_ours(args, w):
         torch.distributed.destroy_process_group()
 
 
+def run_memop(args):
+    """Bench one of the HBM-bound kernels: GB/s against the measured copy bandwidth."""
+    from attention_attn_fwd_05_gb300 import add_rmsnorm, device_status, row_softmax
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    t = torch.float32 if args.dtype == "f32" else torch.bfloat16
+    g = torch.Generator().manual_seed(7)
+    rows, width = args.rows, args.width
+    x = torch.randn(rows, width, generator=g).to(t).to(dev)
+    if args.op == "row_softmax":
+        if t != torch.float32:
+            raise SystemExit("row_softmax is fp32")
+        y = torch.empty_like(x)
+        lse = None
+
+        def step():
+            row_softmax(x, out=y)
+        nbytes = 2 * x.numel() * 4  # read x once, write y once
+        kname = "row_softmax_kernel"
+    else:
+        r = torch.randn(rows, width, generator=g).to(t).to(dev)
+        w = torch.randn(width, generator=g).to(t).to(dev)
+        out, ho = torch.empty_like(x), torch.empty_like(x)
+
+        def step():
+            add_rmsnorm(x, w, r, 1e-6, out=out, res_out=ho)
+        nbytes = 4 * x.numel() * x.element_size() + w.numel() * w.element_size()
+        kname = "add_rmsnorm_kernel"
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index or 0) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if device_status(device=dev) != 0:
+        raise RuntimeError("device status reports a timeout")
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, src = load_peaks()
+    line = {"metric": f"{args.op} GB/s (algorithmic bytes)", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+            "data": "synthetic",
+            "config": {"workload": f"{args.op}_{args.dtype}_rows{rows}_width{width}",
+                       "rows": rows, "width": width,
+                       "l2": "inputs and outputs larger than L2, no flush"
+                       if nbytes > 2 * L2_BYTES else "smaller than L2: L2-resident"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": kname,
+                         "peak_source": f"{src} copy bandwidth (MEASURED_PEAKS.json)",
+                         "algorithmic_bytes_per_launch": nbytes},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -349,7 +411,15 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="attn", choices=["attn", "row_softmax", "add_rmsnorm"],
+                    help="attn (the hot path, default) or one of the HBM-bound kernels")
+    ap.add_argument("--rows", type=int, default=16384)
+    ap.add_argument("--width", type=int, default=8192)
+    ap.add_argument("--dtype", default="bf16", choices=["f32", "bf16"])
     args = ap.parse_args(argv)
+    if args.op != "attn":
+        run_memop(args)
+        return
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -128,6 +128,32 @@ attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,
                              int64_t width, void *stream);
 
 /*
+ * attn_add_rmsnorm -- fused residual add + RMSNorm (page "14. Triton and
+ * kernel fusion", section "Fused residual add + RMSNorm"; the RMSNorm formula
+ * of page "TritonForge"):
+ *
+ *     h       = x + residual          (h = x when residual is NULL)
+ *     out     = h / sqrt(mean_c h_c^2 + eps) * weight
+ *     res_out = h                     (written only with a residual)
+ *
+ *   x, residual   [rows, width] inputs in `dtype` (device, read only);
+ *                 residual may be NULL.
+ *   weight        [width] scale in `dtype` (device, read only).
+ *   out           [rows, width] output in `dtype` (device, fully overwritten).
+ *   res_out       [rows, width] output in `dtype`, required with a residual,
+ *                 ignored without one.  out and res_out must not overlap the
+ *                 inputs.
+ *   rows, width   >= 1, width < 2^31.  eps >= 0 added to the mean square.
+ *   dtype         ATTN_F32 or ATTN_BF16; arithmetic is fp32 either way and bf16
+ *                 outputs are rounded (nearest even) once, on store.
+ * All pointers 16-byte aligned device memory.  Returns ATTN_OK or a
+ * validation / launch error (as attn_fwd).
+ */
+attn_status attn_add_rmsnorm(const void *x, const void *residual, const void *weight, void *out,
+                             void *res_out, int64_t rows, int64_t width, float eps, int dtype,
+                             void *stream);
+
+/*
  * attn_device_status -- synchronise `stream`, then return and clear the
  * current device's status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT if any
  * kernel of this library gave up a bounded wait since the last read.

@@ -24,6 +24,8 @@ Parity status per function (what pins it, in ``tests/test_oracle.py``):
 * ``online_replay``        pinned: equals the one-shot result for tile sizes
                            1, 2, N/2, N and the hand two-tile example.
 * ``row_softmax``          pinned: closed forms and a library cross-check.
+* ``add_rmsnorm``          pinned: constant rows, a hand-worked row, scale
+                           invariance, and a library cross-check.
 """
 from __future__ import annotations
 
@@ -87,10 +89,12 @@ def _load():
                                              _f64p, _f64p]
         lib.oracle_row_softmax.argtypes = [_f32p, _i64, _i64, _f64p, _f64p,
                                            ctypes.c_int]
+        lib.oracle_add_rmsnorm.argtypes = [_f32p, ctypes.c_void_p, _f32p, _i64, _i64,
+                                           ctypes.c_double, _f64p, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_attn_fwd", "oracle_attn_fwd_rows", "oracle_probs_row",
                      "oracle_online_replay", "oracle_row_softmax",
-                     "oracle_max_threads"):
+                     "oracle_add_rmsnorm", "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -191,3 +195,24 @@ def row_softmax(x, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError("oracle_row_softmax failed")
     return y, lse
+
+
+def add_rmsnorm(x, residual, weight, eps: float, nthreads: int = 0):
+    """Residual add + RMSNorm: (out [rows, width], h = x + residual) in float64."""
+    x = _as_f32(x)
+    if x.ndim != 2:
+        raise ValueError("add_rmsnorm expects a matrix")
+    rows, width = x.shape
+    w = _as_f32(weight).reshape(-1)
+    if w.shape[0] != width:
+        raise ValueError("weight must have one entry per column")
+    r = None if residual is None else _as_f32(residual)
+    if r is not None and r.shape != x.shape:
+        raise ValueError("residual must match x")
+    out = np.empty((rows, width), np.float64)
+    h = np.empty((rows, width), np.float64)
+    rc = _load().oracle_add_rmsnorm(x, None if r is None else r.ctypes.data, w, rows, width,
+                                    float(eps), out, h.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_add_rmsnorm failed")
+    return out, h

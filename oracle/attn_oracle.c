@@ -282,3 +282,43 @@ int oracle_row_softmax(const float *x, int64_t rows, int64_t width,
     }
     return 0;
 }
+
+/*
+ * Residual add + RMSNorm of a [rows, width] matrix (page "14. Triton and
+ * kernel fusion", section "Fused residual add + RMSNorm"; the normalisation
+ * of page "TritonForge": x / sqrt(sum x_i^2 / d + eps) * gamma):
+ *     h   = x + residual           (h = x when residual is NULL)
+ *     out = h / sqrt(mean_c h_c^2 + eps) * weight
+ * h_out (may be NULL) receives h.  All in double.
+ */
+int oracle_add_rmsnorm(const float *x, const float *residual, const float *weight,
+                       int64_t rows, int64_t width, double eps, double *out, double *h_out,
+                       int nthreads)
+{
+    if (rows < 1 || width < 1 || !x || !weight || !out)
+        return -1;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        double *h = (double *)malloc((size_t)width * sizeof(double));
+        if (h) {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < rows; ++r) {
+                double ss = 0.0;
+                for (int64_t c = 0; c < width; ++c) {
+                    h[c] = (double)x[r * width + c] +
+                           (residual ? (double)residual[r * width + c] : 0.0);
+                    ss += h[c] * h[c];
+                }
+                const double inv = 1.0 / sqrt(ss / (double)width + eps);
+                for (int64_t c = 0; c < width; ++c) {
+                    out[r * width + c] = h[c] * inv * (double)weight[c];
+                    if (h_out)
+                        h_out[r * width + c] = h[c];
+                }
+            }
+            free(h);
+        }
+    }
+    return 0;
+}

@@ -103,3 +103,14 @@ def test_python_wrapper_value_errors():
         attn_fwd(x, x, x)  # CPU tensors
     with pytest.raises(ValueError):
         row_softmax(torch.zeros(3, 4))
+
+
+def test_add_rmsnorm_validation(L):
+    f = ctypes.c_float(1e-6)
+    assert L.attn_add_rmsnorm(None, None, A, A, None, 1, 8, f, 0, None) == 1
+    assert L.attn_add_rmsnorm(A, A, A, A, None, 1, 8, f, 0, None) == 1   # residual needs res_out
+    assert L.attn_add_rmsnorm(A, None, A, A, None, 0, 8, f, 0, None) == 2
+    assert L.attn_add_rmsnorm(A, None, A, A, None, 1, 0, f, 0, None) == 2
+    assert L.attn_add_rmsnorm(A, None, A, A, None, 1, 2 ** 31, f, 0, None) == 2
+    assert L.attn_add_rmsnorm(A, None, A, A, None, 1, 8, f, 5, None) == 3
+    assert L.attn_add_rmsnorm(A + 4, None, A, A, None, 1, 8, f, 0, None) == 5

@@ -275,3 +275,36 @@ def test_row_softmax_closed_forms_and_library():
     xt = torch.from_numpy(xr).to(torch.float64)
     np.testing.assert_allclose(y, torch.softmax(xt, -1).numpy(), rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(lse, torch.logsumexp(xt, -1).numpy(), rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------- add + rmsnorm ---
+
+def test_add_rmsnorm_closed_forms():
+    """A constant row c normalises to sign(c)*w (up to eps); a hand-worked row
+    [3, 4] has mean square 12.5; the residual is added before the statistic."""
+    w = np.array([1.0, 2.0], np.float32)
+    x = np.array([[3.0, 4.0], [2.0, 2.0]], np.float32)
+    out, h = oracle.add_rmsnorm(x, None, w, 0.0)
+    np.testing.assert_allclose(out[0], [3 / math.sqrt(12.5), 8 / math.sqrt(12.5)], rtol=1e-15)
+    np.testing.assert_allclose(out[1], [1.0, 2.0], rtol=1e-15)
+    r = np.array([[1.0, -1.0], [0.0, 0.0]], np.float32)
+    out, h = oracle.add_rmsnorm(x, r, w, 0.5)
+    np.testing.assert_array_equal(h[0], [4.0, 3.0])
+    np.testing.assert_allclose(out[0], [4 / math.sqrt(13.0), 6 / math.sqrt(13.0)], rtol=1e-15)
+
+
+def test_add_rmsnorm_scale_invariance_and_library():
+    """Without eps, scaling a row leaves its output unchanged; with eps it
+    matches a float64 library computation."""
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(9, 77, generator=g)
+    r = torch.randn(9, 77, generator=g)
+    w = torch.randn(77, generator=g)
+    o1, _ = oracle.add_rmsnorm(x, r, w, 0.0)
+    o2, _ = oracle.add_rmsnorm(4 * x, 4 * r, w, 0.0)
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-14)
+    out, h = oracle.add_rmsnorm(x, r, w, 1e-6)
+    h64 = x.double() + r.double()
+    ref = h64 * torch.rsqrt(h64.pow(2).mean(-1, keepdim=True) + 1e-6) * w.double()
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(h, h64.numpy(), rtol=0, atol=0)
