@@ -6,9 +6,10 @@ for bf16; exact fp32 FMA on CUDA cores for fp32) behind a C ABI
 (``include/attn_fwd.h``).  This package is the thin Python binding over that
 library plus the seeded input generators.
 """
-from .binding import (AttnError, AttnGraph, add_rmsnorm, attn_fwd, attn_fwd_host,
-                      device_status, lib, row_softmax, selftest_wait_timeout)
+from .binding import (AttnError, AttnGraph, Attention, add_rmsnorm, attention, attn_bwd,
+                      attn_fwd, attn_fwd_host, device_status, lib, row_softmax,
+                      selftest_wait_timeout)
 from .build import build
 
-__all__ = ["AttnError", "AttnGraph", "add_rmsnorm", "attn_fwd", "attn_fwd_host", "device_status",
+__all__ = ["AttnError", "AttnGraph", "Attention", "add_rmsnorm", "attention", "attn_bwd", "attn_fwd", "attn_fwd_host", "device_status",
            "lib", "row_softmax", "selftest_wait_timeout", "build"]

@@ -24,7 +24,7 @@ STATUS_NAMES = {
     4: "ATTN_ERR_HEADDIM", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_ARCH", 7: "ATTN_ERR_LAUNCH",
     8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
 }
-EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_add_rmsnorm", "attn_device_status",
+EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_row_softmax", "attn_add_rmsnorm", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_last_cuda_error", "attn_status_string",
             "attn_version")
 
@@ -59,6 +59,8 @@ def lib():
                                ctypes.c_int, ctypes.c_int, vp]
         L.attn_fwd_noalloc.argtypes = list(L.attn_fwd.argtypes)
         L.attn_row_softmax.argtypes = [vp, vp, vp, i64, i64, vp]
+        L.attn_bwd.argtypes = [vp] * 10 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                          ctypes.c_int, vp]
         L.attn_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_float,
                                        ctypes.c_int, vp]
         L.attn_device_status.argtypes = [vp]
@@ -68,7 +70,8 @@ def lib():
         L.attn_status_string.argtypes = [ctypes.c_int]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
-        for name in ("attn_fwd", "attn_fwd_noalloc", "attn_row_softmax", "attn_add_rmsnorm",
+        for name in ("attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_row_softmax",
+                     "attn_add_rmsnorm",
                      "attn_device_status",
                      "attn_selftest_wait_timeout", "attn_version"):
             getattr(L, name).restype = ctypes.c_int
@@ -217,6 +220,56 @@ def row_softmax(x: torch.Tensor, out: Optional[torch.Tensor] = None,
                                     x.shape[0], x.shape[1], _stream_handle(stream, x.device))
     _check(st, "attn_row_softmax")
     return (out, lse) if return_lse else out
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, dout: torch.Tensor, scale: Optional[float] = None,
+             causal: bool = False, stream: Optional[torch.cuda.Stream] = None):
+    """Gradients (dQ, dK, dV) of attn_fwd given its O and LSE and the output gradient."""
+    ts = (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout))
+    for name, t in ts:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q's shape and dtype")
+    if q.dim() != 4:
+        raise ValueError("tensors must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    code = _dtype_code(q.dtype)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            dout.data_ptr(), lse.data_ptr(), delta.data_ptr(), dq.data_ptr(),
+                            dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale),
+                            int(bool(causal)), code, _stream_handle(stream, q.device))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+class Attention(torch.autograd.Function):
+    """Autograd wrapper: forward = attn_fwd, backward = attn_bwd (saved O and LSE)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale=None, causal=False):
+        o, lse = attn_fwd(q.contiguous(), k.contiguous(), v.contiguous(), scale, causal)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale, ctx.causal = scale, causal
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, o, lse, dout.contiguous(), ctx.scale, ctx.causal)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, scale: Optional[float] = None, causal: bool = False):
+    """Differentiable exact attention: softmax(scale Q K^T [causal]) V."""
+    return Attention.apply(q, k, v, scale, causal)
 
 
 def add_rmsnorm(x: torch.Tensor, weight: torch.Tensor, residual: Optional[torch.Tensor] = None,

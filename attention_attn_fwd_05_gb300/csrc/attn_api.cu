@@ -143,6 +143,32 @@ extern "C" attn_status attn_row_softmax(const float *x, float *y, float *lse, in
     return launch_row_softmax(x, y, lse, rows, width, make_ctx(*s, stream, kDefaultTimeoutNs));
 }
 
+extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                                const void *dout, const float *lse, float *delta, void *dq,
+                                void *dk, void *dv, int64_t B, int64_t H, int64_t N, int64_t d,
+                                float scale, int causal, int dtype, void *stream) {
+    if (!q || !k || !v || !o || !dout || !lse || !delta || !dq || !dk || !dv)
+        return ATTN_ERR_NULL;
+    if (B < 1 || H < 1 || N < 1 || N > INT32_MAX || !product_fits(B, H, N, d > 0 ? d : 1))
+        return ATTN_ERR_SHAPE;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+    if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+    if (B * H > 65535) return ATTN_ERR_SHAPE;
+    for (const void *p : {q, k, v, o, dout, static_cast<const void *>(lse),
+                          static_cast<const void *>(delta), static_cast<const void *>(dq),
+                          static_cast<const void *>(dk), static_cast<const void *>(dv)})
+        if (!aligned16(p)) return ATTN_ERR_ALIGN;
+    DeviceState *s = nullptr;
+    attn_status st = device_state(&s);
+    if (st != ATTN_OK) return st;
+    for (const void *p : {q, k, v, o, dout, static_cast<const void *>(lse),
+                          static_cast<const void *>(delta), static_cast<const void *>(dq),
+                          static_cast<const void *>(dk), static_cast<const void *>(dv)})
+        if ((st = check_device_ptr(p)) != ATTN_OK) return st;
+    return launch_attn_bwd(q, k, v, o, dout, lse, delta, dq, dk, dv, B * H, N, (int)d, scale,
+                           causal != 0, dtype, make_ctx(*s, stream, kDefaultTimeoutNs));
+}
+
 extern "C" attn_status attn_add_rmsnorm(const void *x, const void *residual, const void *weight,
                                         void *out, void *res_out, int64_t rows, int64_t width,
                                         float eps, int dtype, void *stream) {

@@ -30,6 +30,12 @@ attn_status launch_attn_fwd_f32(const float *q, const float *k, const float *v, 
 attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t rows, int64_t width,
                                const LaunchCtx &ctx);
 
+// Attention backward (attn_bwd.cu).
+attn_status launch_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse, float *delta, void *dq, void *dk,
+                            void *dv, int64_t BH, int64_t N, int d, float scale, bool causal,
+                            int dtype, const LaunchCtx &ctx);
+
 // Residual add + RMSNorm (add_rmsnorm.cu).
 attn_status launch_add_rmsnorm(const void *x, const void *residual, const void *weight, void *out,
                                void *res_out, int64_t rows, int64_t width, float eps, int dtype,

@@ -401,6 +401,47 @@ def run_memop(args):
         print(json.dumps(line), flush=True)
 
 
+def run_bwd(args, w):
+    """Bench the CUDA-core backward: TFLOP/s with FLOP = 10*B*H*N^2*d (the five
+    N x N x d products of the backward; halved with the causal mask) against
+    the fp32 FMA-pipe peak."""
+    from attention_attn_fwd_05_gb300 import attn_bwd, attn_fwd, device_status
+    dev = torch.device("cuda", 0)
+    q, k, v = (t.to(dev) for t in make_workload_inputs(w))
+    o, lse = attn_fwd(q, k, v, w.scale, w.causal)
+    g = torch.randn(q.shape, generator=torch.Generator().manual_seed(9)).to(q.dtype).to(dev)
+
+    def step():
+        attn_bwd(q, k, v, o, lse, g, w.scale, w.causal)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize(dev)
+    if device_status(device=dev) != 0:
+        raise RuntimeError("device status reports a timeout")
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 10.0 * w.B * w.H * w.N * w.N * w.d / (2 if w.causal else 1)
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks, _ = load_peaks()
+    alu_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    print(json.dumps({
+        "metric": "attention backward TFLOP/s (10*B*H*N^2*d, causal halved)", "value": tf,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic", "config": config_of(w),
+        "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": tf / alu_peak, "traffic": None,
+                     "kernel": "bwd_dkdv_kernel + bwd_dq_kernel",
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"},
+        "gpu_launches": 3 * args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,12 +452,16 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="attn", choices=["attn", "row_softmax", "add_rmsnorm"],
+    ap.add_argument("--op", default="attn",
+                    choices=["attn", "attn_bwd", "row_softmax", "add_rmsnorm"],
                     help="attn (the hot path, default) or one of the HBM-bound kernels")
     ap.add_argument("--rows", type=int, default=16384)
     ap.add_argument("--width", type=int, default=8192)
     ap.add_argument("--dtype", default="bf16", choices=["f32", "bf16"])
     args = ap.parse_args(argv)
+    if args.op == "attn_bwd":
+        run_bwd(args, WORKLOADS[args.workload])
+        return
     if args.op != "attn":
         run_memop(args)
         return

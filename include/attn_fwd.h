@@ -128,6 +128,30 @@ attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,
                              int64_t width, void *stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd: dQ, dK, dV from Q, K, V, the forward's O
+ * and LSE, and dO.  The pages give no attention backward; this is the exact
+ * derivative of the forward formula:
+ *     P_ij = exp(scale q_i.k_j - LSE_i) (0 for masked keys),  D_i = dO_i . O_i,
+ *     dS_ij = P_ij (dO_i . v_j - D_i),
+ *     dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+ * Computed in fp32 on CUDA cores (no atomics: one pass over key groups for
+ * dK and dV, one over query groups for dQ).
+ *
+ *   q, k, v, o, dout   [B,H,N,d] in `dtype` (device, read only); o is the
+ *                      forward's output.
+ *   lse                [B,H,N] fp32 from the forward (device, read only).
+ *   delta              [B,H,N] fp32 workspace owned by the caller (device,
+ *                      overwritten with D); the call allocates nothing.
+ *   dq, dk, dv         [B,H,N,d] outputs in `dtype` (device, fully overwritten).
+ *   B, H, N, d, scale, causal, dtype, stream   as attn_fwd; B*H <= 65535.
+ * All pointers 16-byte aligned.  Returns ATTN_OK or a validation / launch error.
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                     const void *dout, const float *lse, float *delta, void *dq, void *dk,
+                     void *dv, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                     int causal, int dtype, void *stream);
+
+/*
  * attn_add_rmsnorm -- fused residual add + RMSNorm (page "14. Triton and
  * kernel fusion", section "Fused residual add + RMSNorm"; the RMSNorm formula
  * of page "TritonForge"):

@@ -24,6 +24,9 @@ Parity status per function (what pins it, in ``tests/test_oracle.py``):
 * ``online_replay``        pinned: equals the one-shot result for tile sizes
                            1, 2, N/2, N and the hand two-tile example.
 * ``row_softmax``          pinned: closed forms and a library cross-check.
+* ``attn_bwd``             pinned: central finite differences of the oracle
+                           forward, a float64 library autograd cross-check,
+                           and dV = P^T dO row sums.
 * ``add_rmsnorm``          pinned: constant rows, a hand-worked row, scale
                            invariance, and a library cross-check.
 """
@@ -91,10 +94,13 @@ def _load():
                                            ctypes.c_int]
         lib.oracle_add_rmsnorm.argtypes = [_f32p, ctypes.c_void_p, _f32p, _i64, _i64,
                                            ctypes.c_double, _f64p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_attn_bwd.argtypes = [_f32p, _f32p, _f32p, _f32p, _f32p, _f32p,
+                                        _i64, _i64, _i64, _i64, ctypes.c_double, ctypes.c_int,
+                                        _f64p, _f64p, _f64p, ctypes.c_int]
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_attn_fwd", "oracle_attn_fwd_rows", "oracle_probs_row",
                      "oracle_online_replay", "oracle_row_softmax",
-                     "oracle_add_rmsnorm", "oracle_max_threads"):
+                     "oracle_add_rmsnorm", "oracle_attn_bwd", "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -216,3 +222,23 @@ def add_rmsnorm(x, residual, weight, eps: float, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError("oracle_add_rmsnorm failed")
     return out, h
+
+
+def attn_bwd(q, k, v, o, dout, lse, scale: float, causal: bool = False, nthreads: int = 0):
+    """Gradients (dQ, dK, dV) in float64, given the forward's O and LSE."""
+    arrs = [_as_f32(t) for t in (q, k, v, o, dout)]
+    lse = _as_f32(lse)
+    shape = arrs[0].shape
+    if len(shape) != 4 or any(a.shape != shape for a in arrs):
+        raise ValueError("q, k, v, o, dout must share a [B, H, N, d] shape")
+    B, H, N, d = shape
+    if lse.shape != (B, H, N):
+        raise ValueError("lse must be [B, H, N]")
+    dq = np.empty(shape, np.float64)
+    dk = np.empty(shape, np.float64)
+    dv = np.empty(shape, np.float64)
+    rc = _load().oracle_attn_bwd(*arrs, lse, B, H, N, d, float(scale), int(bool(causal)),
+                                 dq, dk, dv, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd failed")
+    return dq, dk, dv

@@ -322,3 +322,69 @@ int oracle_add_rmsnorm(const float *x, const float *residual, const float *weigh
     }
     return 0;
 }
+
+/*
+ * Attention backward over one (batch, head) slice, the exact gradient of the
+ * forward formula given the forward's outputs O and LSE:
+ *     P_ij  = exp(scale q_i.k_j - LSE_i)        (0 for masked keys)
+ *     D_i   = sum_c dO_ic O_ic
+ *     dP_ij = dO_i . v_j
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale sum_j dS_ij k_j
+ *     dK_j  = scale sum_i dS_ij q_i
+ *     dV_j  = sum_i P_ij dO_i
+ * The pages give no attention backward; this is the plain derivative.  All
+ * arrays are one slice, [N, d] (lse [N]); outputs are double.
+ */
+static int bwd_slice(const float *q, const float *k, const float *v, const float *o,
+                     const float *dout, const float *lse, int64_t N, int64_t d, double scale,
+                     int causal, double *dq, double *dk, double *dv)
+{
+    memset(dk, 0, (size_t)(N * d) * sizeof(double));
+    memset(dv, 0, (size_t)(N * d) * sizeof(double));
+    for (int64_t i = 0; i < N; ++i) {
+        const int64_t nvis = causal ? i + 1 : N;
+        double Di = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            Di += (double)dout[i * d + c] * (double)o[i * d + c];
+        for (int64_t c = 0; c < d; ++c)
+            dq[i * d + c] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+            double s = 0.0, dp = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                s += (double)q[i * d + c] * (double)k[j * d + c];
+                dp += (double)dout[i * d + c] * (double)v[j * d + c];
+            }
+            const double pij = exp(scale * s - (double)lse[i]);
+            const double ds = pij * (dp - Di);
+            for (int64_t c = 0; c < d; ++c) {
+                dq[i * d + c] += scale * ds * (double)k[j * d + c];
+                dk[j * d + c] += scale * ds * (double)q[i * d + c];
+                dv[j * d + c] += pij * (double)dout[i * d + c];
+            }
+        }
+    }
+    return 0;
+}
+
+/* Backward for all slices of [B, H, N, d] tensors (OpenMP over slices). */
+int oracle_attn_bwd(const float *q, const float *k, const float *v, const float *o,
+                    const float *dout, const float *lse, int64_t B, int64_t H, int64_t N,
+                    int64_t d, double scale, int causal, double *dq, double *dk, double *dv,
+                    int nthreads)
+{
+    if (bad_shape(B, H, N, d) || !q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+        return -1;
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const int64_t base = bh * N * d;
+        if (bwd_slice(q + base, k + base, v + base, o + base, dout + base, lse + bh * N, N, d,
+                      scale, causal, dq + base, dk + base, dv + base) != 0) {
+#pragma omp atomic write
+            failed = 1;
+        }
+    }
+    return failed ? -1 : 0;
+}

@@ -114,3 +114,16 @@ def test_add_rmsnorm_validation(L):
     assert L.attn_add_rmsnorm(A, None, A, A, None, 1, 2 ** 31, f, 0, None) == 2
     assert L.attn_add_rmsnorm(A, None, A, A, None, 1, 8, f, 5, None) == 3
     assert L.attn_add_rmsnorm(A + 4, None, A, A, None, 1, 8, f, 0, None) == 5
+
+
+def test_attn_bwd_validation(L):
+    f = ctypes.c_float(0.125)
+    args = [A] * 10
+    assert L.attn_bwd(None, *args[1:], 1, 1, 8, 64, f, 0, 1, None) == 1
+    assert L.attn_bwd(*args, 0, 1, 8, 64, f, 0, 1, None) == 2
+    assert L.attn_bwd(*args, 1, 1, 8, 64, f, 0, 9, None) == 3
+    assert L.attn_bwd(*args, 1, 1, 8, 96, f, 0, 1, None) == 4
+    assert L.attn_bwd(*args, 65536, 1, 8, 64, f, 0, 1, None) == 2
+    bad = list(args)
+    bad[6] = A + 4
+    assert L.attn_bwd(*bad, 1, 1, 8, 64, f, 0, 1, None) == 5
