@@ -5,14 +5,18 @@
 // the online normalisation applied per key tile), in plain fp32 FMA with
 // accurate expf/logf, for fp32 inputs and outputs.
 //
-// Layout of the work: TPR threads share one query row, each owning D/TPR of
-// its head dimensions (in 16-byte chunks interleaved across the TPR threads so
-// that shared-memory reads of a key row are conflict-free broadcasts).  A CTA
-// of 128 threads covers 128/TPR rows; K and V tiles of BC keys are staged in
-// shared memory with a two-buffer cp.async pipeline.  Per key tile each thread
-// forms partial dot products for its dimensions, the TPR partials are summed
-// with shuffles, then the running maximum / sum / output update follows the
-// online recurrence.
+// A CTA of 128 threads owns BR = 32 query rows and walks key tiles of BC = 64
+// keys.  The threads form an 8 x 16 grid (ty, tx):
+//   S = Q K^T    thread (ty, tx) computes rows 4ty..4ty+3 x keys 4tx..4tx+3
+//                from Q^T and K^T staged in shared memory (per dimension c:
+//                two 16-byte loads, 16 FMAs; each logit is one sequential
+//                fp32 dot product over c = 0..d-1);
+//   softmax      row max and row sum combine the 16 threads of a row with
+//                shuffles (the 16 threads of a row are one half-warp), so
+//                every exponential is computed exactly once;
+//   O += P V     P^T goes to shared memory; the same thread owns rows
+//                4ty..4ty+3 x columns {4tx + 64k} of O, so the row rescale
+//                factor is already in its registers.
 #include <cmath>
 
 #include "attn_internal.h"
@@ -21,167 +25,166 @@ namespace attn {
 namespace f32 {
 
 constexpr int NUM_THREADS = 128;
+constexpr int BR = 32;  // query rows per CTA
+constexpr int BC = 64;  // keys per tile
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
-    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    const int n = valid ? 16 : 0;  // zero-fill rows past N
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_1() {
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_0() {
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Keys per shared-memory tile: 32 KB of K and V double buffers either way.
 template <int D>
-constexpr int kBC = (D == 128) ? 16 : 32;
+struct Smem {
+    float qt[D][BR];   // Q^T
+    float kt[D][BC];   // K^T
+    float v[BC][D];    // V
+    float pt[BC][BR];  // P^T
+};
 
-template <int D, int TPR>
+template <int D>
 __global__ void __launch_bounds__(NUM_THREADS)
     attn_fwd_f32_kernel(const float *__restrict__ Q, const float *__restrict__ K,
                         const float *__restrict__ V, float *__restrict__ O,
                         float *__restrict__ LSE, int N, float scale, int causal) {
-    constexpr int BC = kBC<D>;
-    constexpr int ROWS = NUM_THREADS / TPR;  // query rows per CTA
-    constexpr int NCH = D / 4 / TPR;         // float4 chunks per thread
-    constexpr int TILE_F4 = BC * D / 4;      // float4s per K (or V) tile
-    __shared__ __align__(16) float Ks[2][BC * D];
-    __shared__ __align__(16) float Vs[2][BC * D];
-
+    constexpr int OC = D / 64;  // float4 column groups of O per thread
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     const int bh = blockIdx.y;
-    const int row0 = blockIdx.x * ROWS;
-    const int lr = threadIdx.x / TPR;
-    const int part = threadIdx.x % TPR;
-    const int row = row0 + lr;
-    const bool valid = row < N;
+    const int row0 = blockIdx.x * BR;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const size_t base = (size_t)bh * (size_t)N * D;
-    const float *Kh = K + base;
-    const float *Vh = V + base;
 
-    // Chunk ci of this thread covers dims [4*(ci*TPR + part), +4).
-    float q[NCH * 4], o[NCH * 4];
-#pragma unroll
-    for (int ci = 0; ci < NCH; ++ci) {
+    // Q^T, zero rows past N.
+    for (int idx = threadIdx.x; idx < BR * (D / 4); idx += NUM_THREADS) {
+        const int r = idx % BR, c4 = idx / BR;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid)
-            x = *reinterpret_cast<const float4 *>(Q + base + (size_t)row * D +
-                                                  4 * (ci * TPR + part));
-        q[4 * ci + 0] = x.x;
-        q[4 * ci + 1] = x.y;
-        q[4 * ci + 2] = x.z;
-        q[4 * ci + 3] = x.w;
-        o[4 * ci + 0] = o[4 * ci + 1] = o[4 * ci + 2] = o[4 * ci + 3] = 0.f;
+        if (row0 + r < N) x = *reinterpret_cast<const float4 *>(Q + base + (size_t)(row0 + r) * D + 4 * c4);
+        sm.qt[4 * c4 + 0][r] = x.x;
+        sm.qt[4 * c4 + 1][r] = x.y;
+        sm.qt[4 * c4 + 2][r] = x.z;
+        sm.qt[4 * c4 + 3][r] = x.w;
     }
 
-    // Keys this CTA needs: all N, or up to its last row with the causal mask.
-    const int kv_end = causal ? min(N, row0 + ROWS) : N;
-    const int ntiles = (kv_end + BC - 1) / BC;
-    const int limit = causal ? min(N, row + 1) : N;  // keys [0, limit) visible to this row
-
-    auto load_tile = [&](int tile, int buf) {
-        const int k0 = tile * BC;
-        for (int i = threadIdx.x; i < TILE_F4; i += NUM_THREADS) {
-            const int kr = i / (D / 4), c4 = i % (D / 4);
-            const bool ok = k0 + kr < N;
-            const size_t off = (size_t)(ok ? k0 + kr : 0) * D + 4 * c4;
-            cp_async16(&Ks[buf][kr * D + 4 * c4], Kh + off, ok);
-            cp_async16(&Vs[buf][kr * D + 4 * c4], Vh + off, ok);
-        }
-        cp_async_commit();
-    };
-
-    float m = -INFINITY, l = 0.f;
-    if (ntiles > 0) load_tile(0, 0);
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int buf = tile & 1;
-        if (tile + 1 < ntiles) {
-            load_tile(tile + 1, buf ^ 1);
-            cp_async_wait_1();
-        } else {
-            cp_async_wait_0();
+    float m[4], l[4], o[4][OC * 4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < OC * 4; ++c) o[i][c] = 0.f;
+    }
+    const int kv_end = causal ? min(N, row0 + BR) : N;
+    for (int k0 = 0; k0 < kv_end; k0 += BC) {
+        __syncthreads();  // previous tile's readers are done
+        for (int idx = threadIdx.x; idx < BC * (D / 4); idx += NUM_THREADS) {
+            const int kr = idx % BC, c4 = idx / BC;
+            float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
+            if (k0 + kr < N) {
+                const size_t off = base + (size_t)(k0 + kr) * D + 4 * c4;
+                kx = *reinterpret_cast<const float4 *>(K + off);
+                vx = *reinterpret_cast<const float4 *>(V + off);
+            }
+            sm.kt[4 * c4 + 0][kr] = kx.x;
+            sm.kt[4 * c4 + 1][kr] = kx.y;
+            sm.kt[4 * c4 + 2][kr] = kx.z;
+            sm.kt[4 * c4 + 3][kr] = kx.w;
+            *reinterpret_cast<float4 *>(&sm.v[kr][4 * c4]) = vx;
         }
         __syncthreads();
 
-        const float *Kt = Ks[buf];
-        const float *Vt = Vs[buf];
-        float s[BC];
+        float s[4][4];
 #pragma unroll
-        for (int j = 0; j < BC; ++j) {
-            float acc = 0.f;
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int ci = 0; ci < NCH; ++ci) {
-                const float4 kv =
-                    *reinterpret_cast<const float4 *>(Kt + j * D + 4 * (ci * TPR + part));
-                acc = fmaf(q[4 * ci + 0], kv.x, acc);
-                acc = fmaf(q[4 * ci + 1], kv.y, acc);
-                acc = fmaf(q[4 * ci + 2], kv.z, acc);
-                acc = fmaf(q[4 * ci + 3], kv.w, acc);
+            for (int jj = 0; jj < 4; ++jj) s[i][jj] = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < D; ++c) {
+            const float4 qv = *reinterpret_cast<const float4 *>(&sm.qt[c][4 * ty]);
+            const float4 kv = *reinterpret_cast<const float4 *>(&sm.kt[c][4 * tx]);
+            const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+            const float ka[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) s[i][jj] = fmaf(qa[i], ka[jj], s[i][jj]);
+        }
+
+        float alpha[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = row0 + 4 * ty + i;
+            const int limit = causal ? min(N, row + 1) : N;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int key = k0 + 4 * tx + jj;
+                s[i][jj] = key < limit ? s[i][jj] * scale : -INFINITY;
+                mx = fmaxf(mx, s[i][jj]);
             }
-            s[j] = acc;
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(m[i], mx);  // finite: key 0 is visible to every row
+            alpha[i] = expf(m[i] - m_new);
+            float rs = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                s[i][jj] = expf(s[i][jj] - m_new);
+                rs += s[i][jj];
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
+            l[i] = l[i] * alpha[i] + rs;
+            m[i] = m_new;
         }
 #pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1) {
+        for (int jj = 0; jj < 4; ++jj)
+            *reinterpret_cast<float4 *>(&sm.pt[4 * tx + jj][4 * ty]) =
+                make_float4(s[0][jj], s[1][jj], s[2][jj], s[3][jj]);
+        __syncthreads();
+
 #pragma unroll
-            for (int j = 0; j < BC; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j], off);
-        }
-        const int k0 = tile * BC;
-        float mx = m;
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < BC; ++j) {
-            s[j] = (k0 + j < limit) ? s[j] * scale : -INFINITY;
-            mx = fmaxf(mx, s[j]);
-        }
-        // Every row sees key 0 in the first tile, so mx is finite from here on.
-        const float alpha = expf(m - mx);
-        l *= alpha;
+            for (int c = 0; c < OC * 4; ++c) o[i][c] *= alpha[i];
+        const int nk = min(BC, kv_end - k0);
+        for (int kk = 0; kk < nk; ++kk) {
+            const float4 pv = *reinterpret_cast<const float4 *>(&sm.pt[kk][4 * ty]);
+            const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-        for (int i = 0; i < NCH * 4; ++i) o[i] *= alpha;
+            for (int g = 0; g < OC; ++g) {
+                const float4 vv = *reinterpret_cast<const float4 *>(&sm.v[kk][64 * g + 4 * tx]);
 #pragma unroll
-        for (int j = 0; j < BC; ++j) {
-            const float p = expf(s[j] - mx);
-            l += p;
-#pragma unroll
-            for (int ci = 0; ci < NCH; ++ci) {
-                const float4 vv =
-                    *reinterpret_cast<const float4 *>(Vt + j * D + 4 * (ci * TPR + part));
-                o[4 * ci + 0] = fmaf(p, vv.x, o[4 * ci + 0]);
-                o[4 * ci + 1] = fmaf(p, vv.y, o[4 * ci + 1]);
-                o[4 * ci + 2] = fmaf(p, vv.z, o[4 * ci + 2]);
-                o[4 * ci + 3] = fmaf(p, vv.w, o[4 * ci + 3]);
+                for (int i = 0; i < 4; ++i) {
+                    o[i][4 * g + 0] = fmaf(pa[i], vv.x, o[i][4 * g + 0]);
+                    o[i][4 * g + 1] = fmaf(pa[i], vv.y, o[i][4 * g + 1]);
+                    o[i][4 * g + 2] = fmaf(pa[i], vv.z, o[i][4 * g + 2]);
+                    o[i][4 * g + 3] = fmaf(pa[i], vv.w, o[i][4 * g + 3]);
+                }
             }
         }
-        m = mx;
-        __syncthreads();  // this buffer is refilled two tiles later
     }
 
-    if (valid) {
-        const float inv_l = 1.f / l;
 #pragma unroll
-        for (int ci = 0; ci < NCH; ++ci) {
-            float4 y;
-            y.x = o[4 * ci + 0] * inv_l;
-            y.y = o[4 * ci + 1] * inv_l;
-            y.z = o[4 * ci + 2] * inv_l;
-            y.w = o[4 * ci + 3] * inv_l;
-            *reinterpret_cast<float4 *>(O + base + (size_t)row * D + 4 * (ci * TPR + part)) = y;
-        }
-        if (LSE != nullptr && part == 0) LSE[(size_t)bh * N + row] = m + logf(l);
+    for (int i = 0; i < 4; ++i) {
+        const int row = row0 + 4 * ty + i;
+        if (row >= N) continue;
+        const float inv_l = 1.f / l[i];
+#pragma unroll
+        for (int g = 0; g < OC; ++g)
+            *reinterpret_cast<float4 *>(O + base + (size_t)row * D + 64 * g + 4 * tx) =
+                make_float4(o[i][4 * g + 0] * inv_l, o[i][4 * g + 1] * inv_l,
+                            o[i][4 * g + 2] * inv_l, o[i][4 * g + 3] * inv_l);
+        if (LSE != nullptr && tx == 0) LSE[(size_t)bh * N + row] = m[i] + logf(l[i]);
     }
 }
 
-template <int D, int TPR>
+template <int D>
 static attn_status launch(const float *q, const float *k, const float *v, float *o, float *lse,
                           int64_t BH, int64_t N, float scale, bool causal, const LaunchCtx &ctx) {
-    constexpr int ROWS = NUM_THREADS / TPR;
-    dim3 grid((unsigned)((N + ROWS - 1) / ROWS), (unsigned)BH);
-    attn_fwd_f32_kernel<D, TPR><<<grid, NUM_THREADS, 0, ctx.stream>>>(q, k, v, o, lse, (int)N,
-                                                                       scale, causal ? 1 : 0);
+    const int smem = (int)sizeof(Smem<D>);
+    if (check_launch(cudaFuncSetAttribute(attn_fwd_f32_kernel<D>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                     ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    dim3 grid((unsigned)((N + BR - 1) / BR), (unsigned)BH);
+    attn_fwd_f32_kernel<D><<<grid, NUM_THREADS, smem, ctx.stream>>>(q, k, v, o, lse, (int)N,
+                                                                     scale, causal ? 1 : 0);
     return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 
@@ -190,8 +193,8 @@ static attn_status launch(const float *q, const float *k, const float *v, float 
 attn_status launch_attn_fwd_f32(const float *q, const float *k, const float *v, float *o,
                                 float *lse, int64_t BH, int64_t N, int d, float scale,
                                 bool causal, const LaunchCtx &ctx) {
-    if (d == 64) return f32::launch<64, 4>(q, k, v, o, lse, BH, N, scale, causal, ctx);
-    if (d == 128) return f32::launch<128, 4>(q, k, v, o, lse, BH, N, scale, causal, ctx);
+    if (d == 64) return f32::launch<64>(q, k, v, o, lse, BH, N, scale, causal, ctx);
+    if (d == 128) return f32::launch<128>(q, k, v, o, lse, BH, N, scale, causal, ctx);
     return ATTN_ERR_HEADDIM;
 }
 
