@@ -10,10 +10,14 @@
 // of one (batch, head) and walks the key tiles j = 0 .. T-1 (up to the
 // diagonal with the causal mask).  Both tiles share every K and V tile.
 //
-//   warp 8      TMA producer: Q_A and Q_B once, then K_0, V_0, K_1, V_1, ...
-//               into a ring of NSLOT shared-memory slots (128-byte swizzle,
-//               64-column boxes).  Slots come back when tile B's softmax sees
-//               S_B(j) complete (see softmax_warpgroup).
+//   warp 8      TMA producer: initialises the barriers and issues Q_A, K_0,
+//               Q_B, V_0 (each query tile on its own barrier, so S_A(0) waits
+//               only for Q_A and K_0) before the CTA-wide barrier, which lets
+//               those copies overlap the TMEM allocation; it also warms L2
+//               with the query block of the CTA that will start next.  Then
+//               K_1, V_1, K_2, ... into a ring of NSLOT shared-memory slots
+//               (128-byte swizzle, 64-column boxes).  Slots come back when
+//               tile B's softmax sees S_B(j) complete (see softmax_warpgroup).
 //   warp 9      TMEM allocator and MMA issuer (one thread).  Per key tile j it
 //               issues, in this order,
 //                 S_A(j) = Q_A K_j^T,  O_B += P_B(j-1) V_{j-1},
@@ -77,8 +81,8 @@ struct Cfg {
     // as bf16 pairs), O_A, O_B (D each).
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
     // Barrier slots (8 bytes each).
-    static constexpr int B_Q = 0;
-    static constexpr int B_FULL = 1;
+    static constexpr int B_Q = 0;     // [2] Q_A, Q_B landed
+    static constexpr int B_FULL = 2;
     static constexpr int B_EMPTY = B_FULL + NSLOT;
     static constexpr int B_SFULL = B_EMPTY + NSLOT;  // [2]
     static constexpr int B_PFULL = B_SFULL + 2;      // [2]
@@ -233,25 +237,28 @@ __device__ __forceinline__ void softmax_warpgroup(
         tc_fence_after();
         const float inv_l = 1.f / l_run;
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(tO + c, o);
-            tmem_wait_ld_x32(o);
+        for (int c = 0; c < D; c += 64) {
+            uint32_t o[2][32];
+            tmem_ld_32x32b_x32(tO + c, o[0]);
+            tmem_ld_32x32b_x32(tO + c + 32, o[1]);
+            tmem_wait_ld_x32(o[0]);
+            tmem_wait_ld_x32(o[1]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const int dcol = c + i * 8;
                 const uint32_t chunk = (uint32_t)(dcol & 63) >> 3;
                 const uint32_t addr = sStage + (dcol >> 6) * (BM * 128) + t * 128 +
                                       ((chunk ^ ((uint32_t)t & 7u)) << 4);
+                const uint32_t *v = &o[i >> 2][(i & 3) * 8];
                 st_shared_v4(addr,
-                             pack_bf16x2(__uint_as_float(o[i * 8 + 0]) * inv_l,
-                                         __uint_as_float(o[i * 8 + 1]) * inv_l),
-                             pack_bf16x2(__uint_as_float(o[i * 8 + 2]) * inv_l,
-                                         __uint_as_float(o[i * 8 + 3]) * inv_l),
-                             pack_bf16x2(__uint_as_float(o[i * 8 + 4]) * inv_l,
-                                         __uint_as_float(o[i * 8 + 5]) * inv_l),
-                             pack_bf16x2(__uint_as_float(o[i * 8 + 6]) * inv_l,
-                                         __uint_as_float(o[i * 8 + 7]) * inv_l));
+                             pack_bf16x2(__uint_as_float(v[0]) * inv_l,
+                                         __uint_as_float(v[1]) * inv_l),
+                             pack_bf16x2(__uint_as_float(v[2]) * inv_l,
+                                         __uint_as_float(v[3]) * inv_l),
+                             pack_bf16x2(__uint_as_float(v[4]) * inv_l,
+                                         __uint_as_float(v[5]) * inv_l),
+                             pack_bf16x2(__uint_as_float(v[6]) * inv_l,
+                                         __uint_as_float(v[7]) * inv_l));
             }
         }
         if (lse != nullptr && row < N)
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const __grid_constant__ CUtensorMap tmV,
                             const __grid_constant__ CUtensorMap tmO, float *__restrict__ lse,
                             int N, int num_cta_tiles, float scale_log2, int causal,
-                            uint32_t *status, uint64_t timeout_ns) {
+                            uint32_t *status, uint64_t timeout_ns, int num_sms) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -296,20 +303,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int TA, TB;
     tile_counts(N, cta_tile, causal, TA, TB);
 
-    if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_Q), 1);
-        for (int s = 0; s < C::NSLOT; ++s) {
-            mbar_init(bar(C::B_FULL + s), 1);
-            mbar_init(bar(C::B_EMPTY + s), 1);
-        }
+    const uint32_t sQ_ = sQ;
+    auto load_q = [&](int x) {
+        mbar_arrive_expect_tx(bar(C::B_Q + x), C::Q_BYTES);
+        for (int c = 0; c < C::DBLK; ++c)
+            tma_load_3d(sQ_ + x * C::Q_BYTES + c * (BM * 128), &tmQ, c * 64, row0 + x * BM, bh,
+                        bar(C::B_Q + x));
+    };
+    auto load_kv = [&](int n) {  // load n of the sequence K_0, V_0, K_1, ... into slot n % NSLOT
+        const int s = n % C::NSLOT;
+        mbar_arrive_expect_tx(bar(C::B_FULL + s), C::SLOT_BYTES);
+        for (int c = 0; c < C::DBLK; ++c)
+            tma_load_3d(sKV + s * C::SLOT_BYTES + c * (BN * 128), (n & 1) ? &tmV : &tmK, c * 64,
+                        (n >> 1) * BN, bh, bar(C::B_FULL + s));
+    };
+    if (warp == WARP_TMA && lane == 0) {
+        // The producer sets up the barriers itself and starts the first copies
+        // before the CTA-wide barrier, so they overlap the TMEM allocation:
+        // Q_A and K_0 first (all S_A(0) needs), then Q_B and V_0.
         for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(C::B_Q + x), 1);
             mbar_init(bar(C::B_SFULL + x), 1);
             mbar_init(bar(C::B_PFULL + x), BM);
             mbar_init(bar(C::B_ODONE + x), 1);
         }
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), 1);
+        }
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0u;
         fence_mbar_init();
+        load_q(0);
+        load_kv(0);
+        load_q(1);
+        load_kv(1);
+        // Warm L2 with the query block of the CTA that will most likely start
+        // next on a free SM (blocks are dispatched in launch order, so that is
+        // the one num_sms further on).
+        const int next = ((int)blockIdx.y * (int)gridDim.x + (int)blockIdx.x) + num_sms;
+        if (next < (int)(gridDim.x * gridDim.y)) {
+            const int nbh = next % (int)gridDim.x, ny = next / (int)gridDim.x;
+            const int ntile = causal ? (num_cta_tiles - 1 - ny) : ny;
+            for (int x = 0; x < 2; ++x) {
+                const int r = ntile * (2 * BM) + x * BM;
+                if (r < N)
+                    for (int c = 0; c < C::DBLK; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, r, nbh);
+            }
+        }
     }
     if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -324,28 +365,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_TMA) {
         // ------------------------------------------------------ producer ---
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::Q_BYTES);
-            for (int x = 0; x < 2; ++x)
-                for (int c = 0; c < C::DBLK; ++c)
-                    tma_load_3d(sQ + x * C::Q_BYTES + c * (BM * 128), &tmQ, c * 64,
-                                row0 + x * BM, bh, bar(C::B_Q));
-            // Load sequence K_0, V_0, K_1, V_1, ...: load n goes to slot n % NSLOT.
-            int n = 0;
+            // Loads 0 and 1 (K_0, V_0) were issued before the CTA-wide barrier.
+            int n = 2;
             for (; n < 2 * TB; ++n) {
                 const int s = n % C::NSLOT;
                 if (n >= C::NSLOT &&
                     !bounded_wait(bar(C::B_EMPTY + s), ((n / C::NSLOT) - 1) & 1, ctl))
                     break;
-                const uint32_t dst = sKV + s * C::SLOT_BYTES;
-                const CUtensorMap *tm = (n & 1) ? &tmV : &tmK;
-                mbar_arrive_expect_tx(bar(C::B_FULL + s), C::SLOT_BYTES);
-                for (int c = 0; c < C::DBLK; ++c)
-                    tma_load_3d(dst + c * (BN * 128), tm, c * 64, (n >> 1) * BN, bh,
-                                bar(C::B_FULL + s));
+                load_kv(n);
             }
             // Let the copies issued last land before exiting (already complete
             // on the normal path).
-            drain_wait(bar(C::B_Q), 0, timeout_ns);
+            drain_wait(bar(C::B_Q + 0), 0, timeout_ns);
+            drain_wait(bar(C::B_Q + 1), 0, timeout_ns);
             for (int i = (n > C::NSLOT ? n - C::NSLOT : 0); i < n; ++i)
                 drain_wait(bar(C::B_FULL + i % C::NSLOT), (i / C::NSLOT) & 1, timeout_ns);
         }
@@ -379,7 +411,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + (x ? C::TM_S1 : C::TM_S0),
                            sdesc_sw128(sV, BN * 128, 1024), idesc_o, first ? 0u : 1u);
             };
-            bool ok = bounded_wait(bar(C::B_Q), 0, ctl);
+            bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl);
             for (int j = 0; ok && j < TB; ++j) {
                 const int nK = 2 * j;
                 if (!(ok = wait_full(nK))) break;
@@ -393,6 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     issue_pv(1, slot_addr(nV), j == 1);
                 }
+                if (j == 0 && !(ok = bounded_wait(bar(C::B_Q + 1), 0, ctl))) break;
                 issue_s(1, slot_addr(nK));
                 if (j < TA) {
                     const int nV = 2 * j + 1;
@@ -502,7 +535,7 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
     dim3 grid((unsigned)BH, (unsigned)num_cta_tiles);
     attn_fwd_bf16_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
         tq, tk, tv, to, lse, (int)N, num_cta_tiles, scale_log2, causal ? 1 : 0, ctx.status,
-        ctx.timeout_ns);
+        ctx.timeout_ns, ctx.sm_count);
     return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 
