@@ -238,6 +238,18 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     if device_status(device=dev) != 0:
         raise RuntimeError("device status reports a timeout during warm-up")
+    # Device memory the call itself takes (driver view, so any allocation inside
+    # the library would show), beside what materialising the scores would take.
+    free0 = torch.cuda.mem_get_info(dev)[0]
+    step()
+    torch.cuda.synchronize(dev)
+    extra = max(0, free0 - torch.cuda.mem_get_info(dev)[0])
+    scores = w.B * w.H * w.N * w.N * 4
+    memory = {"extra_device_bytes_per_call": extra, "io_bytes": w.io_bytes,
+              "scores_fp32_bytes": scores,
+              "eager_peak_bytes": w.io_bytes + 2 * scores,
+              "reduction_vs_eager": 1.0 - (w.io_bytes + extra) / (w.io_bytes + 2 * scores),
+              "eager_model": "inputs, outputs, S and P materialised in fp32"}
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -332,6 +344,7 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
+        "memory": memory,
         "gpu": torch.cuda.get_device_name(dev),
     }
     print(json.dumps(line), flush=True)
