@@ -5,12 +5,19 @@
 // the online normalisation applied per key tile), in plain fp32 FMA with
 // accurate expf/logf, for fp32 inputs and outputs.
 //
-// A CTA of 128 threads owns BR = 32 query rows and walks key tiles of BC = 64
-// keys.  The threads form an 8 x 16 grid (ty, tx):
-//   S = Q K^T    thread (ty, tx) computes rows 4ty..4ty+3 x keys 4tx..4tx+3
-//                from Q^T and K^T staged in shared memory (per dimension c:
-//                two 16-byte loads, 16 FMAs; each logit is one sequential
-//                fp32 dot product over c = 0..d-1);
+// A CTA owns BR = 32 query rows.  It has G groups of 128 threads (G = 1 or 2,
+// chosen per launch); group g walks the key tiles g, g + G, g + 2G, ... of
+// BC = 64 keys with its own online state, and the G partial states (m, l, O)
+// are merged at the end with the same rescale rule.  Each group streams its K
+// and V tiles through two shared-memory buffers with cp.async, so the copy of
+// tile t+G overlaps the arithmetic on tile t.  A group's threads form an
+// 8 x 16 grid (ty, tx):
+//   S = Q K^T    thread (ty, tx) computes rows 4ty..4ty+3 x keys tx + 16jj
+//                (jj = 0..3) from Q and K rows in shared memory (row-major,
+//                rows padded by 16 bytes so the 16 key rows a half-warp reads
+//                fall in distinct banks); per 4 dimensions: 8 16-byte loads,
+//                64 FMAs; each logit is one sequential fp32 dot product over
+//                c = 0..d-1;
 //   softmax      row max and row sum combine the 16 threads of a row with
 //                shuffles (the 16 threads of a row are one half-warp), so
 //                every exponential is computed exactly once;
@@ -24,84 +31,131 @@
 namespace attn {
 namespace f32 {
 
-constexpr int NUM_THREADS = 128;
+constexpr int GROUP_THREADS = 128;
 constexpr int BR = 32;  // query rows per CTA
 constexpr int BC = 64;  // keys per tile
 
 template <int D>
+struct GroupSmem {
+    float k[2][BC][D + 4];  // K rows, two buffers
+    float v[2][BC][D];      // V rows, two buffers
+    float pt[BC][BR + 4];   // P^T
+};
+template <int D, int G>
 struct Smem {
-    float qt[D][BR];   // Q^T
-    float kt[D][BC];   // K^T
-    float v[BC][D];    // V
-    float pt[BC][BR];  // P^T
+    float q[BR][D + 4];  // Q rows, shared by the groups
+    GroupSmem<D> grp[G];
 };
 
+// Running state of one thread: 4 rows x (4 * D/64) columns of O.
 template <int D>
-__global__ void __launch_bounds__(NUM_THREADS)
+struct RowState {
+    float m[4], l[4], o[4][D / 16];
+};
+
+// 16-byte global -> shared copy; rows past N are zero-filled (no bytes read).
+__device__ __forceinline__ void cp_async16(float *dst, const float *src, bool valid) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <int D, int G>
+__global__ void __launch_bounds__(GROUP_THREADS * G)
     attn_fwd_f32_kernel(const float *__restrict__ Q, const float *__restrict__ K,
                         const float *__restrict__ V, float *__restrict__ O,
                         float *__restrict__ LSE, int N, float scale, int causal) {
     constexpr int OC = D / 64;  // float4 column groups of O per thread
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
+    Smem<D, G> &sm = *reinterpret_cast<Smem<D, G> *>(smem_raw);
+    const int g = threadIdx.x / GROUP_THREADS;  // key-split group
+    GroupSmem<D> &gs = sm.grp[g];
+    const int tid = threadIdx.x % GROUP_THREADS;
     const int bh = blockIdx.y;
     const int row0 = blockIdx.x * BR;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int tx = tid & 15, ty = tid >> 4;
     const size_t base = (size_t)bh * (size_t)N * D;
+    // Each group has its own named barrier (id 1 + g) for its tile loop: the
+    // groups walk different numbers of key tiles.  Immediate ids keep the
+    // CTA's barrier count at G + 1.
+    auto group_sync = [&]() {
+        if (g == 0)
+            asm volatile("bar.sync 1, %0;" ::"n"(GROUP_THREADS) : "memory");
+        else
+            asm volatile("bar.sync 2, %0;" ::"n"(GROUP_THREADS) : "memory");
+    };
+    // Copy key tile k0 (K and V rows, zero past N) into buffer b.
+    auto load_tile = [&](int k0, int b) {
+        for (int idx = tid; idx < BC * (D / 4); idx += GROUP_THREADS) {
+            const int kr = idx / (D / 4), c4 = idx % (D / 4);
+            const bool ok = k0 + kr < N;
+            const size_t off = ok ? base + (size_t)(k0 + kr) * D + 4 * c4 : 0;
+            cp_async16(&gs.k[b][kr][4 * c4], K + off, ok);
+            cp_async16(&gs.v[b][kr][4 * c4], V + off, ok);
+        }
+    };
 
-    // Q^T, zero rows past N.
-    for (int idx = threadIdx.x; idx < BR * (D / 4); idx += NUM_THREADS) {
-        const int r = idx % BR, c4 = idx / BR;
+    const int kv_end = causal ? min(N, row0 + BR) : N;
+    // Group g takes key tiles g, g + G, g + 2G, ...: each group runs the
+    // online recurrence over its own subset of keys, and the partial states
+    // are merged at the end (the same max/rescale rule applied once more).
+    int k0 = g * BC;
+    if (k0 < kv_end) load_tile(k0, 0);
+    cp_async_commit();
+
+    // Q rows, zero past N (plain loads; they overlap the first tile's copy).
+    for (int idx = threadIdx.x; idx < BR * (D / 4); idx += GROUP_THREADS * G) {
+        const int r = idx / (D / 4), c4 = idx % (D / 4);
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row0 + r < N) x = *reinterpret_cast<const float4 *>(Q + base + (size_t)(row0 + r) * D + 4 * c4);
-        sm.qt[4 * c4 + 0][r] = x.x;
-        sm.qt[4 * c4 + 1][r] = x.y;
-        sm.qt[4 * c4 + 2][r] = x.z;
-        sm.qt[4 * c4 + 3][r] = x.w;
+        *reinterpret_cast<float4 *>(&sm.q[r][4 * c4]) = x;
     }
+    __syncthreads();
 
-    float m[4], l[4], o[4][OC * 4];
+    RowState<D> st;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        m[i] = -INFINITY;
-        l[i] = 0.f;
+        st.m[i] = -INFINITY;
+        st.l[i] = 0.f;
 #pragma unroll
-        for (int c = 0; c < OC * 4; ++c) o[i][c] = 0.f;
+        for (int c = 0; c < OC * 4; ++c) st.o[i][c] = 0.f;
     }
-    const int kv_end = causal ? min(N, row0 + BR) : N;
-    for (int k0 = 0; k0 < kv_end; k0 += BC) {
-        __syncthreads();  // previous tile's readers are done
-        for (int idx = threadIdx.x; idx < BC * (D / 4); idx += NUM_THREADS) {
-            const int kr = idx % BC, c4 = idx / BC;
-            float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
-            if (k0 + kr < N) {
-                const size_t off = base + (size_t)(k0 + kr) * D + 4 * c4;
-                kx = *reinterpret_cast<const float4 *>(K + off);
-                vx = *reinterpret_cast<const float4 *>(V + off);
-            }
-            sm.kt[4 * c4 + 0][kr] = kx.x;
-            sm.kt[4 * c4 + 1][kr] = kx.y;
-            sm.kt[4 * c4 + 2][kr] = kx.z;
-            sm.kt[4 * c4 + 3][kr] = kx.w;
-            *reinterpret_cast<float4 *>(&sm.v[kr][4 * c4]) = vx;
-        }
-        __syncthreads();
+    for (int t = 0; k0 < kv_end; ++t, k0 += G * BC) {
+        const int b = t & 1;
+        // Everyone is done with buffer b^1 (the previous tile): refill it with
+        // the next tile while this one is used.
+        group_sync();
+        if (k0 + G * BC < kv_end) load_tile(k0 + G * BC, b ^ 1);
+        cp_async_commit();
+        cp_async_wait_1();  // this thread's copies of tile t have landed
+        group_sync();       // ... and everyone else's
 
         float s[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) s[i][jj] = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < D; ++c) {
-            const float4 qv = *reinterpret_cast<const float4 *>(&sm.qt[c][4 * ty]);
-            const float4 kv = *reinterpret_cast<const float4 *>(&sm.kt[c][4 * tx]);
-            const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
-            const float ka[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll 4
+        for (int c = 0; c < D; c += 4) {
+            float4 qv[4], kv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4 *>(&sm.q[4 * ty + i][c]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                kv[jj] = *reinterpret_cast<const float4 *>(&gs.k[b][tx + 16 * jj][c]);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) s[i][jj] = fmaf(qa[i], ka[jj], s[i][jj]);
+                for (int jj = 0; jj < 4; ++jj) {
+                    float a = s[i][jj];
+                    a = fmaf(qv[i].x, kv[jj].x, a);
+                    a = fmaf(qv[i].y, kv[jj].y, a);
+                    a = fmaf(qv[i].z, kv[jj].z, a);
+                    s[i][jj] = fmaf(qv[i].w, kv[jj].w, a);
+                }
         }
 
         float alpha[4];
@@ -112,80 +166,159 @@ __global__ void __launch_bounds__(NUM_THREADS)
             float mx = -INFINITY;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                const int key = k0 + 4 * tx + jj;
+                const int key = k0 + tx + 16 * jj;
                 s[i][jj] = key < limit ? s[i][jj] * scale : -INFINITY;
                 mx = fmaxf(mx, s[i][jj]);
             }
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1)
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(m[i], mx);  // finite: key 0 is visible to every row
-            alpha[i] = expf(m[i] - m_new);
+            // A tile can be fully masked for a row (a group's later tiles with
+            // the causal mask); the max then stays where it was.
+            const float m_new = fmaxf(st.m[i], mx);
+            const float m_ref = m_new == -INFINITY ? 0.f : m_new;
+            alpha[i] = expf(st.m[i] - m_ref);
             float rs = 0.f;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                s[i][jj] = expf(s[i][jj] - m_new);
+                s[i][jj] = expf(s[i][jj] - m_ref);
                 rs += s[i][jj];
             }
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
-            l[i] = l[i] * alpha[i] + rs;
-            m[i] = m_new;
+            st.l[i] = st.l[i] * alpha[i] + rs;
+            st.m[i] = m_new;
         }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
-            *reinterpret_cast<float4 *>(&sm.pt[4 * tx + jj][4 * ty]) =
+            *reinterpret_cast<float4 *>(&gs.pt[tx + 16 * jj][4 * ty]) =
                 make_float4(s[0][jj], s[1][jj], s[2][jj], s[3][jj]);
-        __syncthreads();
+        group_sync();
 
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int c = 0; c < OC * 4; ++c) o[i][c] *= alpha[i];
+            for (int c = 0; c < OC * 4; ++c) st.o[i][c] *= alpha[i];
         const int nk = min(BC, kv_end - k0);
+#pragma unroll 4
         for (int kk = 0; kk < nk; ++kk) {
-            const float4 pv = *reinterpret_cast<const float4 *>(&sm.pt[kk][4 * ty]);
+            const float4 pv = *reinterpret_cast<const float4 *>(&gs.pt[kk][4 * ty]);
             const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-            for (int g = 0; g < OC; ++g) {
-                const float4 vv = *reinterpret_cast<const float4 *>(&sm.v[kk][64 * g + 4 * tx]);
+            for (int gg = 0; gg < OC; ++gg) {
+                const float4 vv = *reinterpret_cast<const float4 *>(&gs.v[b][kk][64 * gg + 4 * tx]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    o[i][4 * g + 0] = fmaf(pa[i], vv.x, o[i][4 * g + 0]);
-                    o[i][4 * g + 1] = fmaf(pa[i], vv.y, o[i][4 * g + 1]);
-                    o[i][4 * g + 2] = fmaf(pa[i], vv.z, o[i][4 * g + 2]);
-                    o[i][4 * g + 3] = fmaf(pa[i], vv.w, o[i][4 * g + 3]);
+                    st.o[i][4 * gg + 0] = fmaf(pa[i], vv.x, st.o[i][4 * gg + 0]);
+                    st.o[i][4 * gg + 1] = fmaf(pa[i], vv.y, st.o[i][4 * gg + 1]);
+                    st.o[i][4 * gg + 2] = fmaf(pa[i], vv.z, st.o[i][4 * gg + 2]);
+                    st.o[i][4 * gg + 3] = fmaf(pa[i], vv.w, st.o[i][4 * gg + 3]);
                 }
             }
         }
     }
 
+    if constexpr (G > 1) {
+        // Merge: group 1 parks its state in its own K area (free once the
+        // CTA-wide barrier below has passed), laid out [field][thread] so each
+        // access is coalesced; group 0 folds it into its own with the same
+        // rescale rule.
+        constexpr int NF = 8 + 4 * (D / 16);
+        static_assert(NF * GROUP_THREADS * sizeof(float) <= sizeof(float) * 2 * BC * (D + 4),
+                      "merge area too small");
+        __syncthreads();
+        if (g == 1) {
+            float *park = &gs.k[0][0][0];
+            const float *f = reinterpret_cast<const float *>(&st);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int row = row0 + 4 * ty + i;
-        if (row >= N) continue;
-        const float inv_l = 1.f / l[i];
+            for (int i = 0; i < NF; ++i) park[i * GROUP_THREADS + tid] = f[i];
+        }
+        __syncthreads();
+        if (g == 0) {
+            const float *park = &sm.grp[1].k[0][0][0];
+            RowState<D> o;
+            float *f = reinterpret_cast<float *>(&o);
 #pragma unroll
-        for (int g = 0; g < OC; ++g)
-            *reinterpret_cast<float4 *>(O + base + (size_t)row * D + 64 * g + 4 * tx) =
-                make_float4(o[i][4 * g + 0] * inv_l, o[i][4 * g + 1] * inv_l,
-                            o[i][4 * g + 2] * inv_l, o[i][4 * g + 3] * inv_l);
-        if (LSE != nullptr && tx == 0) LSE[(size_t)bh * N + row] = m[i] + logf(l[i]);
+            for (int i = 0; i < NF; ++i) f[i] = park[i * GROUP_THREADS + tid];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float m_new = fmaxf(st.m[i], o.m[i]);  // finite: group 0 saw key 0
+                const float a = expf(st.m[i] - m_new), bb = expf(o.m[i] - m_new);
+                st.l[i] = st.l[i] * a + o.l[i] * bb;
+#pragma unroll
+                for (int c = 0; c < OC * 4; ++c) st.o[i][c] = st.o[i][c] * a + o.o[i][c] * bb;
+                st.m[i] = m_new;
+            }
+        }
     }
+
+    if (g == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = row0 + 4 * ty + i;
+            if (row >= N) continue;
+            const float inv_l = 1.f / st.l[i];
+#pragma unroll
+            for (int gg = 0; gg < OC; ++gg)
+                *reinterpret_cast<float4 *>(O + base + (size_t)row * D + 64 * gg + 4 * tx) =
+                    make_float4(st.o[i][4 * gg + 0] * inv_l, st.o[i][4 * gg + 1] * inv_l,
+                                st.o[i][4 * gg + 2] * inv_l, st.o[i][4 * gg + 3] * inv_l);
+            if (LSE != nullptr && tx == 0) LSE[(size_t)bh * N + row] = st.m[i] + logf(st.l[i]);
+        }
+    }
+}
+
+template <int D, int G>
+static attn_status launch_g(const float *q, const float *k, const float *v, float *o, float *lse,
+                            int64_t BH, int64_t N, float scale, bool causal, const LaunchCtx &ctx) {
+    const int smem = (int)sizeof(Smem<D, G>);
+    if (check_launch(cudaFuncSetAttribute(attn_fwd_f32_kernel<D, G>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                     ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    dim3 grid((unsigned)((N + BR - 1) / BR), (unsigned)BH);
+    attn_fwd_f32_kernel<D, G><<<grid, GROUP_THREADS * G, smem, ctx.stream>>>(
+        q, k, v, o, lse, (int)N, scale, causal ? 1 : 0);
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+}
+
+// Number of key-split groups per CTA.  A small grid leaves most of each SM
+// idle while one 4-warp CTA walks its key tiles in series; two groups walk
+// interleaved halves at once.  G is the one that minimises (waves of CTAs) /
+// G, where the CTAs one SM holds follow from the shared memory each needs;
+// ties go to the smaller G, and G never exceeds the number of key tiles.
+template <int D>
+static int pick_groups(int64_t BH, int64_t N, int sm_count) {
+    const int64_t ctas = BH * ((N + BR - 1) / BR);
+    const int64_t key_tiles = (N + BC - 1) / BC;
+    constexpr int64_t kSmemPerSm = 228 * 1024;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int G = 1; G <= 2; ++G) {
+        if (G > 1 && (G > key_tiles || sizeof(Smem<D, 2>) > 227 * 1024)) break;
+        const int64_t bytes = (int64_t)(G == 1 ? sizeof(Smem<D, 1>) : sizeof(Smem<D, 2>)) + 1024;
+        int64_t per_sm = kSmemPerSm / bytes;
+        const int64_t by_threads = 2048 / (GROUP_THREADS * G);
+        if (per_sm > by_threads) per_sm = by_threads;
+        if (per_sm < 1) break;
+        const int64_t slots = per_sm * (int64_t)sm_count;
+        const double cost = (double)((ctas + slots - 1) / slots) / G;
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = G;
+        }
+    }
+    return best;
 }
 
 template <int D>
 static attn_status launch(const float *q, const float *k, const float *v, float *o, float *lse,
                           int64_t BH, int64_t N, float scale, bool causal, const LaunchCtx &ctx) {
-    const int smem = (int)sizeof(Smem<D>);
-    if (check_launch(cudaFuncSetAttribute(attn_fwd_f32_kernel<D>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-                     ATTN_ERR_CUDA) != ATTN_OK)
-        return ATTN_ERR_CUDA;
-    dim3 grid((unsigned)((N + BR - 1) / BR), (unsigned)BH);
-    attn_fwd_f32_kernel<D><<<grid, NUM_THREADS, smem, ctx.stream>>>(q, k, v, o, lse, (int)N,
-                                                                     scale, causal ? 1 : 0);
-    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+    if constexpr (sizeof(Smem<D, 2>) <= 227 * 1024) {
+        if (pick_groups<D>(BH, N, ctx.sm_count) == 2)
+            return launch_g<D, 2>(q, k, v, o, lse, BH, N, scale, causal, ctx);
+    }
+    return launch_g<D, 1>(q, k, v, o, lse, BH, N, scale, causal, ctx);
 }
 
 }  // namespace f32
