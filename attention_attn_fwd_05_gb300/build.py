@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libattn_gb300.so")
 SOURCES = ["attn_api.cu", "attn_fwd_tc.cu", "attn_fwd_f32.cu", "row_softmax.cu",
-           "attn_noalloc.cu", "add_rmsnorm.cu", "attn_bwd.cu"]
+           "attn_noalloc.cu", "add_rmsnorm.cu", "attn_bwd.cu", "attn_bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-cudart", "shared",
               "--expt-relaxed-constexpr"]

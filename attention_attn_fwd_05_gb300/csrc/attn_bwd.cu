@@ -1,4 +1,6 @@
-// attn_bwd.cu -- attention backward on CUDA cores, fp32 arithmetic.
+// attn_bwd.cu -- attention backward on CUDA cores, fp32 arithmetic (the fp32
+// path; bf16 goes to the tensor-core kernels of attn_bwd_tc.cu after the D
+// kernel here).
 //
 // The exact gradient of O = softmax(scale Q K^T) V, using the forward's saved
 // O and LSE (the pages give no attention backward; this is the plain
@@ -15,8 +17,7 @@
 // group of queries, walk their keys and accumulate dQ.  Work layout as in the
 // exact-fp32 forward: TPR threads share a row, each owning D/TPR dimensions
 // in 16-byte chunks interleaved across the TPR threads; tiles of the other
-// operand are staged in shared memory (fp32) and read as broadcasts.  bf16
-// tensors are widened on load and rounded once on store.
+// operand are staged in shared memory (fp32) and read as broadcasts.
 #include <cmath>
 #include <cstdint>
 
@@ -250,6 +251,26 @@ static attn_status launch_t(const void *q, const void *k, const void *v, const v
 
 }  // namespace bwd
 
+attn_status launch_bwd_delta(const void *o, const void *dout, float *delta, int64_t rows, int d,
+                             int dtype, const LaunchCtx &ctx) {
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    if (dtype == ATTN_F32) {
+        const float *O = static_cast<const float *>(o), *G = static_cast<const float *>(dout);
+        if (d == 64)
+            bwd::bwd_delta_kernel<float, 64><<<grid, 256, 0, ctx.stream>>>(O, G, delta, rows);
+        else
+            bwd::bwd_delta_kernel<float, 128><<<grid, 256, 0, ctx.stream>>>(O, G, delta, rows);
+    } else {
+        const uint16_t *O = static_cast<const uint16_t *>(o);
+        const uint16_t *G = static_cast<const uint16_t *>(dout);
+        if (d == 64)
+            bwd::bwd_delta_kernel<uint16_t, 64><<<grid, 256, 0, ctx.stream>>>(O, G, delta, rows);
+        else
+            bwd::bwd_delta_kernel<uint16_t, 128><<<grid, 256, 0, ctx.stream>>>(O, G, delta, rows);
+    }
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+}
+
 attn_status launch_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                             const void *dout, const float *lse, float *delta, void *dq, void *dk,
                             void *dv, int64_t BH, int64_t N, int d, float scale, bool causal,
@@ -261,11 +282,11 @@ attn_status launch_attn_bwd(const void *q, const void *k, const void *v, const v
         return bwd::launch_t<float, 128>(q, k, v, o, dout, lse, delta, dq, dk, dv, BH, N, scale,
                                          causal, ctx);
     }
-    if (d == 64)
-        return bwd::launch_t<uint16_t, 64>(q, k, v, o, dout, lse, delta, dq, dk, dv, BH, N, scale,
-                                           causal, ctx);
-    return bwd::launch_t<uint16_t, 128>(q, k, v, o, dout, lse, delta, dq, dk, dv, BH, N, scale,
-                                        causal, ctx);
+    // bf16: D on CUDA cores, then the two tensor-core kernels (attn_bwd_tc.cu).
+    const attn_status st = launch_bwd_delta(o, dout, delta, BH * N, d, dtype, ctx);
+    if (st != ATTN_OK) return st;
+    return launch_attn_bwd_bf16_tc(q, k, v, dout, lse, delta, dq, dk, dv, BH, N, d, scale, causal,
+                                   ctx);
 }
 
 }  // namespace attn

@@ -1,0 +1,541 @@
+// attn_bwd_tc.cu -- bf16 attention backward on sm_103a tensor cores.
+//
+// The gradient of O = softmax(scale Q K^T) V from the forward's saved LSE (the
+// pages give no attention backward; this is the plain derivative of the
+// forward formula of page "Hardware Acceleration & Custom Kernels", section
+// 2, the same one the CUDA-core backward computes):
+//     P_ij  = exp(scale q_i.k_j - LSE_i)        (0 for masked keys)
+//     D_i   = dO_i . O_i
+//     dS_ij = P_ij (dO_i . v_j - D_i)
+//     dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO.
+//
+// Two kernels, no atomics, both built like the forward kernel (TMA producer
+// warp, one MMA-issuing thread, four warps that own one TMEM lane = one row
+// each):
+//
+//   bwd_dkdv_tc_kernel   one CTA per 128-key block (keys on the TMEM lanes).
+//       K and V stay in shared memory; Q and dO blocks stream through a
+//       two-stage ring.  Per query block:
+//         S^T = K Q^T,  dP^T = V dO^T                  (SS MMAs -> TMEM)
+//         P^T = exp2(S^T scale log2e - LSE log2e),  dS^T = P^T (dP^T - D)
+//                                                     (CUDA cores, bf16 -> TMEM)
+//         dV += P^T dO,  dK += dS^T Q                  (TS MMAs, A from TMEM)
+//   bwd_dq_tc_kernel     one CTA per 128-query block (queries on the lanes).
+//       Q and dO stay; K and V blocks stream.  Per key block:
+//         S = Q K^T,  dP = dO V^T;  dS = P (dP - D);  dQ += dS K.
+//
+// S and dP are recomputed in the second kernel (7 GEMMs where a single pass
+// with atomic dQ updates would do 5) so that every output row has exactly one
+// writer.  P and dS are rounded to bf16 for the MMAs; every sum accumulates
+// in fp32 in TMEM.  TMEM (512 columns): S/P, dP/dS, then dV and dK (or dQ).
+#include <cuda.h>
+
+#include <cmath>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace bwdtc {
+
+constexpr int BM = 128;            // rows of the block a CTA owns
+constexpr int BN = 128;            // rows of a streamed block
+constexpr int NSTAGE = 2;          // ring depth (streamed block pairs)
+constexpr int WARP_TMA = 4;
+constexpr int WARP_MMA = 5;
+constexpr int NUM_THREADS = 192;   // 4 row warps + TMA warp + MMA warp
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float LOG2E = 1.44269504088896340736f;
+
+template <int D>
+struct Cfg {
+    static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+    static constexpr int DBLK = D / 64;                  // 128-byte column blocks per row
+    static constexpr uint32_t TILE = BM * D * 2;          // one 128-row bf16 tile
+    static constexpr uint32_t OFF_RES = 0;                // two resident tiles
+    static constexpr uint32_t OFF_RING = 2 * TILE;        // NSTAGE x two streamed tiles
+    static constexpr uint32_t OFF_VEC = OFF_RING + NSTAGE * 2 * TILE;  // [2 buf][2][BN] floats
+    static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 2 * BN * 4;
+    static constexpr uint32_t BAR_BYTES = 128;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + base alignment slack
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
+    static constexpr int B_RES = 0;                  // resident tiles landed
+    static constexpr int B_FULL = 1;                 // [NSTAGE] streamed pair landed
+    static constexpr int B_EMPTY = B_FULL + NSTAGE;  // [NSTAGE] streamed pair consumed
+    static constexpr int B_SFULL = B_EMPTY + NSTAGE; // S and dP in TMEM
+    static constexpr int B_PFULL = B_SFULL + 1;      // P and dS in TMEM (one arrival per row)
+    static constexpr int B_DONE = B_PFULL + 1;       // every MMA finished
+    static constexpr int NUM_BARS = B_DONE + 1;
+    static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
+    static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+    static_assert(8 * NUM_BARS + 8 <= BAR_BYTES, "barrier area too small");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget exceeded");
+    static_assert(TM_ACC1 + D <= TMEM_COLS, "TMEM budget exceeded");
+};
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+// Row r of a 128-row tile staged in the tensor maps' 128-byte swizzle: 16-byte
+// chunk c (8 bf16) of 64-column block b.
+__device__ __forceinline__ uint32_t swz_addr(uint32_t tile, int r, int col) {
+    const uint32_t chunk = (uint32_t)(col & 63) >> 3;
+    return tile + (uint32_t)(col >> 6) * (BM * 128) + (uint32_t)r * 128 +
+           ((chunk ^ ((uint32_t)r & 7u)) << 4);
+}
+
+// Write a row of D fp32 accumulator columns (times `mul`) as bf16 into a
+// staged tile.
+template <int D>
+__device__ __forceinline__ void stage_row(uint32_t tacc, uint32_t tile, int r, float mul) {
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tacc + c, o);
+        tmem_wait_ld_x32(o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            st_shared_v4(swz_addr(tile, r, c + 8 * i),
+                         pack_bf16x2(__uint_as_float(o[8 * i + 0]) * mul,
+                                     __uint_as_float(o[8 * i + 1]) * mul),
+                         pack_bf16x2(__uint_as_float(o[8 * i + 2]) * mul,
+                                     __uint_as_float(o[8 * i + 3]) * mul),
+                         pack_bf16x2(__uint_as_float(o[8 * i + 4]) * mul,
+                                     __uint_as_float(o[8 * i + 5]) * mul),
+                         pack_bf16x2(__uint_as_float(o[8 * i + 6]) * mul,
+                                     __uint_as_float(o[8 * i + 7]) * mul));
+    }
+}
+
+// dS = P (dP - delta) for one row of 128 columns: P (fp32) is in p[]; dP is
+// read from TMEM 32 columns at a time and dS (bf16 pairs) written back over
+// the first 64 dP columns.  Chunk ch writes columns [16 ch, 16 ch + 16), all
+// of which belong to dP chunks already read.  `dl(c)` gives delta for column c.
+template <typename DeltaFn>
+__device__ __forceinline__ void ds_row(uint32_t tdp, const float (&p)[128], DeltaFn dl) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t g[32];
+        tmem_ld_32x32b_x32(tdp + 32 * ch, g);
+        tmem_wait_ld_x32(g);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = 32 * ch + 2 * i;
+            const float d0 = p[c] * (__uint_as_float(g[2 * i]) - dl(c));
+            const float d1 = p[c + 1] * (__uint_as_float(g[2 * i + 1]) - dl(c + 1));
+            pk[i] = pack_bf16x2(d0, d1);
+        }
+        tmem_st_32x32b_x16(tdp + 16 * ch, pk);
+    }
+}
+
+// --------------------------------------------------------- dK and dV ---
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmG,
+                       const __grid_constant__ CUtensorMap tmDK,
+                       const __grid_constant__ CUtensorMap tmDV, const float *__restrict__ lse,
+                       const float *__restrict__ delta, int N, float scale, int causal,
+                       uint32_t *status, uint64_t timeout_ns) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sK = sbase + C::OFF_RES, sV = sK + C::TILE;
+    auto sQ = [&](int s) -> uint32_t { return sbase + C::OFF_RING + (uint32_t)s * 2 * C::TILE; };
+    auto sG = [&](int s) -> uint32_t { return sQ(s) + C::TILE; };
+    float *vec = reinterpret_cast<float *>(smem + C::OFF_VEC);  // [buf][0: -LSE log2e, 1: D][BN]
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM_SLOT);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_ABORT);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int kb = blockIdx.y;  // key block (small kb = most query blocks with the causal mask)
+    const int nq = (N + BN - 1) / BN;
+    const int q0 = causal ? kb : 0;  // query blocks q0 .. nq-1 see this key block
+    const int T = nq - q0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_RES), 1);
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_PFULL), BM);
+        mbar_init(bar(C::B_DONE), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, status, timeout_ns};
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE);
+            for (int c = 0; c < C::DBLK; ++c) {
+                tma_load_3d(sK + c * (BM * 128), &tmK, c * 64, kb * BM, bh, bar(C::B_RES));
+                tma_load_3d(sV + c * (BM * 128), &tmV, c * 64, kb * BM, bh, bar(C::B_RES));
+            }
+            int t = 0;
+            for (; t < T; ++t) {
+                const int s = t % NSTAGE;
+                if (t >= NSTAGE &&
+                    !bounded_wait(bar(C::B_EMPTY + s), ((t / NSTAGE) - 1) & 1, ctl))
+                    break;
+                const int qr = (q0 + t) * BN;
+                mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
+                for (int c = 0; c < C::DBLK; ++c) {
+                    tma_load_3d(sQ(s) + c * (BN * 128), &tmQ, c * 64, qr, bh, bar(C::B_FULL + s));
+                    tma_load_3d(sG(s) + c * (BN * 128), &tmG, c * 64, qr, bh, bar(C::B_FULL + s));
+                }
+            }
+            drain_wait(bar(C::B_RES), 0, timeout_ns);
+            for (int i = (t > NSTAGE ? t - NSTAGE : 0); i < t; ++i)
+                drain_wait(bar(C::B_FULL + i % NSTAGE), (i / NSTAGE) & 1, timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
+            const uint64_t kdesc = sdesc_sw128(sK, 16, 1024), vdesc = sdesc_sw128(sV, 16, 1024);
+            bool ok = bounded_wait(bar(C::B_RES), 0, ctl);
+            for (int t = 0; ok && t < T; ++t) {
+                const int s = t % NSTAGE;
+                if (!(ok = bounded_wait(bar(C::B_FULL + s), (t / NSTAGE) & 1, ctl))) break;
+                // S^T = K Q^T and dP^T = V dO^T (both operands K-major).
+                if constexpr (D == 128) {
+                    gemm_ss_k8(tmem + C::TM_S, kdesc, sdesc_sw128(sQ(s), 16, 1024), idesc_s, 0u);
+                    gemm_ss_k8(tmem + C::TM_DP, vdesc, sdesc_sw128(sG(s), 16, 1024), idesc_s, 0u);
+                } else {
+                    gemm_ss_k4(tmem + C::TM_S, kdesc, sdesc_sw128(sQ(s), 16, 1024), idesc_s, 0u);
+                    gemm_ss_k4(tmem + C::TM_DP, vdesc, sdesc_sw128(sG(s), 16, 1024), idesc_s, 0u);
+                }
+                mma_commit(bar(C::B_SFULL));
+                if (!(ok = bounded_wait(bar(C::B_PFULL), t & 1, ctl))) break;
+                tc_fence_after();
+                // dV += P^T dO and dK += dS^T Q: A (bf16 pairs) from TMEM, B the
+                // streamed tile read MN-major (d contiguous; the two 64-column
+                // halves BN*128 bytes apart).  The next S^T / dP^T overwrite P^T
+                // / dS^T only after these, in issue order.
+                gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_S, sdesc_sw128(sG(s), BN * 128, 1024),
+                           idesc_o, t > 0 ? 1u : 0u);
+                gemm_ts_k8(tmem + C::TM_ACC1, tmem + C::TM_DP, sdesc_sw128(sQ(s), BN * 128, 1024),
+                           idesc_o, t > 0 ? 1u : 0u);
+                mma_commit(bar(C::B_EMPTY + s));
+            }
+            mma_commit(bar(C::B_DONE));
+            drain_wait(bar(C::B_DONE), 0, timeout_ns);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------- rows: one key per thread ---
+        const int t = threadIdx.x;  // 0..127 == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::TM_S, tDP = tmem + lane_base + C::TM_DP;
+        const int key = kb * BM + t;
+        const float sl = scale * LOG2E;
+        const float *lse_bh = lse + (size_t)bh * (size_t)N;
+        const float *dl_bh = delta + (size_t)bh * (size_t)N;
+        bool ok = true;
+        // All four warps run every step (a failed wait only makes the rest
+        // return at once), so the named barrier below always sees them all.
+        for (int st = 0; st < T; ++st) {
+            const int qb = q0 + st;
+            float *nb = vec + (st & 1) * 2 * BN;  // -LSE log2e per query column
+            float *dv = nb + BN;                 // D per query column
+            const int qi = qb * BN + t;
+            nb[t] = qi < N ? -lse_bh[qi] * LOG2E : -INFINITY;  // rows past N: P = 0
+            dv[t] = qi < N ? dl_bh[qi] : 0.f;
+            named_bar_sync(1, BM);
+            ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL), st & 1, ctl)) && ok;
+            tc_fence_after();
+            uint32_t r[4][32];
+            tmem_ld_32x32b_x32(tS + 0, r[0]);
+            tmem_ld_32x32b_x32(tS + 32, r[1]);
+            tmem_ld_32x32b_x32(tS + 64, r[2]);
+            tmem_ld_32x32b_x32(tS + 96, r[3]);
+            tmem_wait_ld_x32(r[0]);
+            tmem_wait_ld_x32(r[1]);
+            tmem_wait_ld_x32(r[2]);
+            tmem_wait_ld_x32(r[3]);
+            // On the diagonal block, query column c sees this key only if c >= t.
+            const int first_col = (causal && qb == kb) ? t : 0;
+            float p[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const float e = ex2_approx(fmaf(__uint_as_float(r[c >> 5][c & 31]), sl, nb[c]));
+                p[c] = c >= first_col ? e : 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(p[64 * h + 2 * i], p[64 * h + 2 * i + 1]);
+                tmem_st_32x32b_x32(tS + 32 * h, pk);
+            }
+            ds_row(tDP, p, [&](int c) { return dv[c]; });
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));
+        }
+        ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DONE), 0, ctl)) && ok;
+        // K and V are no longer read (every MMA is done): stage dV and dK there.
+        if (ok) {
+            tc_fence_after();
+            stage_row<D>(tmem + lane_base + C::TM_ACC0, sV, t, 1.f);
+            stage_row<D>(tmem + lane_base + C::TM_ACC1, sK, t, scale);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, BM);
+        if (t == 0 && ok && *abort_flag == 0u) {
+            // The tensor maps clip rows >= N.
+            for (int c = 0; c < C::DBLK; ++c) {
+                tma_store_3d(&tmDV, sV + c * (BM * 128), c * 64, kb * BM, bh);
+                tma_store_3d(&tmDK, sK + c * (BM * 128), c * 64, kb * BM, bh);
+            }
+            tma_store_commit();
+            tma_store_wait_read();
+        }
+        (void)key;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- dQ ---
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmDQ, const float *__restrict__ lse,
+                     const float *__restrict__ delta, int N, float scale, int causal,
+                     uint32_t *status, uint64_t timeout_ns) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::OFF_RES, sG = sQ + C::TILE;
+    auto sK = [&](int s) -> uint32_t { return sbase + C::OFF_RING + (uint32_t)s * 2 * C::TILE; };
+    auto sV = [&](int s) -> uint32_t { return sK(s) + C::TILE; };
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM_SLOT);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_ABORT);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int nq = (N + BM - 1) / BM;
+    // Heaviest query blocks first with the causal mask.
+    const int qb = causal ? (nq - 1 - (int)blockIdx.y) : (int)blockIdx.y;
+    const int nk = (N + BN - 1) / BN;
+    const int T = causal ? qb + 1 : nk;  // key blocks 0 .. T-1
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_RES), 1);
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_PFULL), BM);
+        mbar_init(bar(C::B_DONE), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, status, timeout_ns};
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE);
+            for (int c = 0; c < C::DBLK; ++c) {
+                tma_load_3d(sQ + c * (BM * 128), &tmQ, c * 64, qb * BM, bh, bar(C::B_RES));
+                tma_load_3d(sG + c * (BM * 128), &tmG, c * 64, qb * BM, bh, bar(C::B_RES));
+            }
+            int t = 0;
+            for (; t < T; ++t) {
+                const int s = t % NSTAGE;
+                if (t >= NSTAGE &&
+                    !bounded_wait(bar(C::B_EMPTY + s), ((t / NSTAGE) - 1) & 1, ctl))
+                    break;
+                mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
+                for (int c = 0; c < C::DBLK; ++c) {
+                    tma_load_3d(sK(s) + c * (BN * 128), &tmK, c * 64, t * BN, bh, bar(C::B_FULL + s));
+                    tma_load_3d(sV(s) + c * (BN * 128), &tmV, c * 64, t * BN, bh, bar(C::B_FULL + s));
+                }
+            }
+            drain_wait(bar(C::B_RES), 0, timeout_ns);
+            for (int i = (t > NSTAGE ? t - NSTAGE : 0); i < t; ++i)
+                drain_wait(bar(C::B_FULL + i % NSTAGE), (i / NSTAGE) & 1, timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
+            const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024), gdesc = sdesc_sw128(sG, 16, 1024);
+            bool ok = bounded_wait(bar(C::B_RES), 0, ctl);
+            for (int t = 0; ok && t < T; ++t) {
+                const int s = t % NSTAGE;
+                if (!(ok = bounded_wait(bar(C::B_FULL + s), (t / NSTAGE) & 1, ctl))) break;
+                // S = Q K^T and dP = dO V^T.
+                if constexpr (D == 128) {
+                    gemm_ss_k8(tmem + C::TM_S, qdesc, sdesc_sw128(sK(s), 16, 1024), idesc_s, 0u);
+                    gemm_ss_k8(tmem + C::TM_DP, gdesc, sdesc_sw128(sV(s), 16, 1024), idesc_s, 0u);
+                } else {
+                    gemm_ss_k4(tmem + C::TM_S, qdesc, sdesc_sw128(sK(s), 16, 1024), idesc_s, 0u);
+                    gemm_ss_k4(tmem + C::TM_DP, gdesc, sdesc_sw128(sV(s), 16, 1024), idesc_s, 0u);
+                }
+                mma_commit(bar(C::B_SFULL));
+                if (!(ok = bounded_wait(bar(C::B_PFULL), t & 1, ctl))) break;
+                tc_fence_after();
+                // dQ += dS K: A = dS (bf16 pairs in TMEM), B = the K tile read
+                // MN-major (keys along K, d contiguous).
+                gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_DP, sdesc_sw128(sK(s), BN * 128, 1024),
+                           idesc_o, t > 0 ? 1u : 0u);
+                mma_commit(bar(C::B_EMPTY + s));
+            }
+            mma_commit(bar(C::B_DONE));
+            drain_wait(bar(C::B_DONE), 0, timeout_ns);
+        }
+        __syncwarp();
+    } else {
+        // ----------------------------------- rows: one query per thread ---
+        const int t = threadIdx.x;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::TM_S, tDP = tmem + lane_base + C::TM_DP;
+        const int row = qb * BM + t;
+        const float sl = scale * LOG2E;
+        const float nb = row < N ? -lse[(size_t)bh * N + row] * LOG2E : -INFINITY;
+        const float dl = row < N ? delta[(size_t)bh * N + row] : 0.f;
+        const int limit = causal ? min(N, row + 1) : N;  // keys [0, limit) are visible
+        bool ok = true;
+        for (int st = 0; st < T; ++st) {
+            ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL), st & 1, ctl)) && ok;
+            tc_fence_after();
+            uint32_t r[4][32];
+            tmem_ld_32x32b_x32(tS + 0, r[0]);
+            tmem_ld_32x32b_x32(tS + 32, r[1]);
+            tmem_ld_32x32b_x32(tS + 64, r[2]);
+            tmem_ld_32x32b_x32(tS + 96, r[3]);
+            tmem_wait_ld_x32(r[0]);
+            tmem_wait_ld_x32(r[1]);
+            tmem_wait_ld_x32(r[2]);
+            tmem_wait_ld_x32(r[3]);
+            const int key0 = st * BN;
+            float p[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const float e = ex2_approx(fmaf(__uint_as_float(r[c >> 5][c & 31]), sl, nb));
+                p[c] = key0 + c < limit ? e : 0.f;
+            }
+            ds_row(tDP, p, [&](int) { return dl; });
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));
+        }
+        ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DONE), 0, ctl)) && ok;
+        // Q is no longer read: stage dQ there.
+        if (ok) {
+            tc_fence_after();
+            stage_row<D>(tmem + lane_base + C::TM_ACC0, sQ, t, scale);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, BM);
+        if (t == 0 && ok && *abort_flag == 0u) {
+            for (int c = 0; c < C::DBLK; ++c)
+                tma_store_3d(&tmDQ, sQ + c * (BM * 128), c * 64, qb * BM, bh);
+            tma_store_commit();
+            tma_store_wait_read();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+template <int D>
+static attn_status launch(const void *q, const void *k, const void *v, const void *dout,
+                          const float *lse, const float *delta, void *dq, void *dk, void *dv,
+                          int64_t BH, int64_t N, float scale, bool causal, const LaunchCtx &ctx) {
+    using C = Cfg<D>;
+    CUtensorMap tq, tk, tv, tg, tdq, tdk, tdv;
+    if (!make_tmap_bf16(&tq, q, BH, N, D) || !make_tmap_bf16(&tk, k, BH, N, D) ||
+        !make_tmap_bf16(&tv, v, BH, N, D) || !make_tmap_bf16(&tg, dout, BH, N, D) ||
+        !make_tmap_bf16(&tdq, dq, BH, N, D) || !make_tmap_bf16(&tdk, dk, BH, N, D) ||
+        !make_tmap_bf16(&tdv, dv, BH, N, D))
+        return ATTN_ERR_CUDA;
+    if (check_launch(cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)C::SMEM_BYTES),
+                     ATTN_ERR_CUDA) != ATTN_OK ||
+        check_launch(cudaFuncSetAttribute(bwd_dq_tc_kernel<D>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)C::SMEM_BYTES),
+                     ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    const dim3 grid((unsigned)BH, (unsigned)((N + BM - 1) / BM));
+    bwd_dkdv_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
+        tq, tk, tv, tg, tdk, tdv, lse, delta, (int)N, scale, causal ? 1 : 0, ctx.status,
+        ctx.timeout_ns);
+    attn_status st = check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+    if (st != ATTN_OK) return st;
+    bwd_dq_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
+        tq, tk, tv, tg, tdq, lse, delta, (int)N, scale, causal ? 1 : 0, ctx.status,
+        ctx.timeout_ns);
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+}
+
+}  // namespace bwdtc
+
+attn_status launch_attn_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout,
+                                    const float *lse, const float *delta, void *dq, void *dk,
+                                    void *dv, int64_t BH, int64_t N, int d, float scale,
+                                    bool causal, const LaunchCtx &ctx) {
+    if (d == 64)
+        return bwdtc::launch<64>(q, k, v, dout, lse, delta, dq, dk, dv, BH, N, scale, causal, ctx);
+    if (d == 128)
+        return bwdtc::launch<128>(q, k, v, dout, lse, delta, dq, dk, dv, BH, N, scale, causal, ctx);
+    return ATTN_ERR_HEADDIM;
+}
+
+}  // namespace attn

@@ -502,10 +502,13 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
+}  // namespace tc
+
 // [BH, N, d] bf16 tensor as a 3-D map with 64-column x 128-row boxes, 128-byte
 // swizzle; rows beyond N read as zero and are clipped on store.
-static bool make_tmap(CUtensorMap *m, const void *ptr, int64_t BH, int64_t N, int d) {
-    EncodeTiledFn enc = get_encode_fn();
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t BH, int64_t N, int d) {
+    using tc::EncodeTiledFn;
+    EncodeTiledFn enc = tc::get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
@@ -517,13 +520,15 @@ static bool make_tmap(CUtensorMap *m, const void *ptr, int64_t BH, int64_t N, in
     return r == CUDA_SUCCESS;
 }
 
+namespace tc {
+
 template <int D>
 static attn_status launch(const void *q, const void *k, const void *v, void *o, float *lse,
                           int64_t BH, int64_t N, float scale, bool causal, const LaunchCtx &ctx) {
     using C = Cfg<D>;
     CUtensorMap tq, tk, tv, to;
-    if (!make_tmap(&tq, q, BH, N, D) || !make_tmap(&tk, k, BH, N, D) ||
-        !make_tmap(&tv, v, BH, N, D) || !make_tmap(&to, o, BH, N, D))
+    if (!make_tmap_bf16(&tq, q, BH, N, D) || !make_tmap_bf16(&tk, k, BH, N, D) ||
+        !make_tmap_bf16(&tv, v, BH, N, D) || !make_tmap_bf16(&to, o, BH, N, D))
         return ATTN_ERR_CUDA;
     if (check_launch(cudaFuncSetAttribute(attn_fwd_bf16_tc_kernel<D>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/attn_fwd.h"
@@ -29,6 +30,20 @@ attn_status launch_attn_fwd_f32(const float *q, const float *k, const float *v, 
 // Row softmax (row_softmax.cu).
 attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t rows, int64_t width,
                                const LaunchCtx &ctx);
+
+// [BH, N, d] bf16 tensor map with 64-column x 128-row boxes and 128-byte
+// swizzle (attn_fwd_tc.cu); false if the driver entry point or the encode fails.
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t BH, int64_t N, int d);
+
+// D = rowsum(dO * O) for the backward (attn_bwd.cu).
+attn_status launch_bwd_delta(const void *o, const void *dout, float *delta, int64_t rows, int d,
+                             int dtype, const LaunchCtx &ctx);
+
+// bf16 attention backward on tensor cores (attn_bwd_tc.cu); delta must hold D.
+attn_status launch_attn_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout,
+                                    const float *lse, const float *delta, void *dq, void *dk,
+                                    void *dv, int64_t BH, int64_t N, int d, float scale,
+                                    bool causal, const LaunchCtx &ctx);
 
 // Attention backward (attn_bwd.cu).
 attn_status launch_attn_bwd(const void *q, const void *k, const void *v, const void *o,

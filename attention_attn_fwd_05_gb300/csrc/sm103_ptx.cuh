@@ -72,7 +72,7 @@ enum : uint32_t {
 // Slow path of bounded_wait (kept out of line so the fast path stays a
 // single try_wait): keep polling; every 64 polls look at the abort flag, the
 // status word and the clock.
-__device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl ctl) {
+static __device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl ctl) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -415,9 +415,11 @@ def run_memop(args):
 
 
 def run_bwd(args, w):
-    """Bench the CUDA-core backward: TFLOP/s with FLOP = 10*B*H*N^2*d (the five
-    N x N x d products of the backward; halved with the causal mask) against
-    the fp32 FMA-pipe peak."""
+    """Bench the backward: TFLOP/s with FLOP = 10*B*H*N^2*d (the five N x N x d
+    products of the backward; halved with the causal mask).  bf16 runs on the
+    tensor-core kernels (which recompute S and dP for dQ: 14*B*H*N^2*d of MMA
+    work) and is reported against the bf16 peak; fp32 runs on CUDA cores and
+    is reported against the fp32 FMA-pipe peak."""
     from attention_attn_fwd_05_gb300 import attn_bwd, attn_fwd, device_status
     dev = torch.device("cuda", 0)
     q, k, v = (t.to(dev) for t in make_workload_inputs(w))
@@ -441,17 +443,25 @@ def run_bwd(args, w):
     ms = e0.elapsed_time(e1) / args.steps
     flops = 10.0 * w.B * w.H * w.N * w.N * w.d / (2 if w.causal else 1)
     tf = flops / (ms * 1e-3) / 1e12
-    peaks, _ = load_peaks()
-    alu_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    peaks, peak_src = load_peaks()
+    if w.dtype == "bf16":
+        peak = peaks["bf16_tflops_sustained" if ms * args.steps > 1000.0 else "bf16_tflops"]
+        roofline = {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                    "frac": tf / peak, "traffic": None,
+                    "kernel": "bwd_dkdv_tc_kernel + bwd_dq_tc_kernel",
+                    "mma_flops_per_launch": flops * 1.4,
+                    "peak_source": f"{peak_src} bf16 dense (MEASURED_PEAKS.json)"}
+    else:
+        alu_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        roofline = {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s",
+                    "frac": tf / alu_peak, "traffic": None,
+                    "kernel": "bwd_dkdv_kernel + bwd_dq_kernel",
+                    "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"}
     print(json.dumps({
         "metric": "attention backward TFLOP/s (10*B*H*N^2*d, causal halved)", "value": tf,
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic", "config": config_of(w),
-        "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": tf / alu_peak, "traffic": None,
-                     "kernel": "bwd_dkdv_kernel + bwd_dq_kernel",
-                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"},
+        "dtype": w.dtype, "data": "synthetic", "config": config_of(w), "roofline": roofline,
         "gpu_launches": 3 * args.steps, "clocks": clk.summary()}), flush=True)
 
 

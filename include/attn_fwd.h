@@ -134,8 +134,10 @@ attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,
  *     P_ij = exp(scale q_i.k_j - LSE_i) (0 for masked keys),  D_i = dO_i . O_i,
  *     dS_ij = P_ij (dO_i . v_j - D_i),
  *     dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
- * Computed in fp32 on CUDA cores (no atomics: one pass over key groups for
- * dK and dV, one over query groups for dQ).
+ * No atomics: one pass over key blocks for dK and dV, one over query blocks
+ * for dQ.  ATTN_F32: exact fp32 arithmetic on CUDA cores.  ATTN_BF16: tcgen05
+ * tensor cores, S and dP recomputed per block pair, P and dS rounded to bf16
+ * for the products, every sum accumulated in fp32, outputs rounded once.
  *
  *   q, k, v, o, dout   [B,H,N,d] in `dtype` (device, read only); o is the
  *                      forward's output.

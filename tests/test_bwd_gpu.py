@@ -71,3 +71,27 @@ def test_autograd_function_fp32():
     np.testing.assert_allclose(out.detach().cpu().numpy(), ref.detach().numpy(), atol=2e-5, rtol=1e-4)
     for a, b in ((qd, q64), (kd, k64), (vd, v64)):
         np.testing.assert_allclose(a.grad.cpu().numpy(), b.grad.numpy(), atol=2e-4, rtol=1e-3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,dist", [(700, "normal"), (1024, "normal"), (600, "stress")])
+def test_bwd_parity_bf16_multiblock(d, causal, N, dist):
+    """bf16 backward over several 128-row blocks on both the key and the query
+    side, ragged tails, and large logits (variance-16 Q and K)."""
+    q, k, v = make_qkv(1, 2, N, d, seed=900 + N + d, dtype="bf16", dist=dist)
+    scale = float(torch.tensor(1 / math.sqrt(d), dtype=torch.float32))
+    o64, lse64 = oracle.attn_fwd(q, k, v, scale, causal)
+    o = torch.from_numpy(o64).to(torch.bfloat16)
+    lse = torch.from_numpy(lse64).float()
+    g = torch.randn(q.shape, generator=torch.Generator().manual_seed(N + 1)).to(torch.bfloat16)
+    dq, dk, dv = attn_bwd(q.cuda(), k.cuda(), v.cuda(), o.cuda(), lse.cuda(), g.cuda(), scale,
+                          causal)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    rq, rk, rv = oracle.attn_bwd(q, k, v, o, g, lse, scale, causal)
+    mx = lambda t: float(t.float().abs().max())
+    ds_bound = 2 * mx(g) * mx(v)
+    _check("bf16", dq, rq, "dQ", scale * mx(k) * ds_bound)
+    _check("bf16", dk, rk, "dK", scale * mx(q) * ds_bound)
+    _check("bf16", dv, rv, "dV", mx(g))
