@@ -62,9 +62,11 @@ struct Cfg {
     static constexpr int B_RES = 0;                  // resident tiles landed
     static constexpr int B_FULL = 1;                 // [NSTAGE] streamed pair landed
     static constexpr int B_EMPTY = B_FULL + NSTAGE;  // [NSTAGE] streamed pair consumed
-    static constexpr int B_SFULL = B_EMPTY + NSTAGE; // S and dP in TMEM
-    static constexpr int B_PFULL = B_SFULL + 1;      // P and dS in TMEM (one arrival per row)
-    static constexpr int B_DONE = B_PFULL + 1;       // every MMA finished
+    static constexpr int B_SFULL = B_EMPTY + NSTAGE; // S in TMEM
+    static constexpr int B_DPRDY = B_SFULL + 1;      // dP in TMEM
+    static constexpr int B_PFULL = B_DPRDY + 1;      // P in TMEM (dK/dV kernel; one arrival per row)
+    static constexpr int B_DSRDY = B_PFULL + 1;      // dS in TMEM (one arrival per row)
+    static constexpr int B_DONE = B_DSRDY + 1;       // every MMA finished
     static constexpr int NUM_BARS = B_DONE + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
     static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -175,7 +177,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(C::B_EMPTY + s), 1);
         }
         mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_DPRDY), 1);
         mbar_init(bar(C::B_PFULL), BM);
+        mbar_init(bar(C::B_DSRDY), BM);
         mbar_init(bar(C::B_DONE), 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -220,30 +224,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
             const uint64_t kdesc = sdesc_sw128(sK, 16, 1024), vdesc = sdesc_sw128(sV, 16, 1024);
-            bool ok = bounded_wait(bar(C::B_RES), 0, ctl);
+            // S^T = K Q^T and dP^T = V dO^T of query block t (both operands
+            // K-major), each on its own barrier so the row warps start on P^T
+            // while dP^T is still being computed.
+            auto issue_s = [&](int t) {
+                const uint64_t b = sdesc_sw128(sQ(t % NSTAGE), 16, 1024);
+                if constexpr (D == 128)
+                    gemm_ss_k8(tmem + C::TM_S, kdesc, b, idesc_s, 0u);
+                else
+                    gemm_ss_k4(tmem + C::TM_S, kdesc, b, idesc_s, 0u);
+                mma_commit(bar(C::B_SFULL));
+            };
+            auto issue_dp = [&](int t) {
+                const uint64_t b = sdesc_sw128(sG(t % NSTAGE), 16, 1024);
+                if constexpr (D == 128)
+                    gemm_ss_k8(tmem + C::TM_DP, vdesc, b, idesc_s, 0u);
+                else
+                    gemm_ss_k4(tmem + C::TM_DP, vdesc, b, idesc_s, 0u);
+                mma_commit(bar(C::B_DPRDY));
+            };
+            bool ok = bounded_wait(bar(C::B_RES), 0, ctl) && bounded_wait(bar(C::B_FULL), 0, ctl);
+            if (ok) {
+                issue_s(0);
+                issue_dp(0);
+            }
+            // Per block t: dV += P^T dO, then S^T of block t+1 (it overwrites
+            // P^T, after dV in issue order), then dK += dS^T Q, then dP^T of
+            // block t+1 (it overwrites dS^T, after dK).  The row warps' work
+            // on block t overlaps dP^T(t), dV(t) and S^T(t+1).  A (bf16 pairs)
+            // comes from TMEM; B is the streamed tile read MN-major (d
+            // contiguous; the two 64-column halves BN*128 bytes apart).
             for (int t = 0; ok && t < T; ++t) {
                 const int s = t % NSTAGE;
-                if (!(ok = bounded_wait(bar(C::B_FULL + s), (t / NSTAGE) & 1, ctl))) break;
-                // S^T = K Q^T and dP^T = V dO^T (both operands K-major).
-                if constexpr (D == 128) {
-                    gemm_ss_k8(tmem + C::TM_S, kdesc, sdesc_sw128(sQ(s), 16, 1024), idesc_s, 0u);
-                    gemm_ss_k8(tmem + C::TM_DP, vdesc, sdesc_sw128(sG(s), 16, 1024), idesc_s, 0u);
-                } else {
-                    gemm_ss_k4(tmem + C::TM_S, kdesc, sdesc_sw128(sQ(s), 16, 1024), idesc_s, 0u);
-                    gemm_ss_k4(tmem + C::TM_DP, vdesc, sdesc_sw128(sG(s), 16, 1024), idesc_s, 0u);
-                }
-                mma_commit(bar(C::B_SFULL));
                 if (!(ok = bounded_wait(bar(C::B_PFULL), t & 1, ctl))) break;
                 tc_fence_after();
-                // dV += P^T dO and dK += dS^T Q: A (bf16 pairs) from TMEM, B the
-                // streamed tile read MN-major (d contiguous; the two 64-column
-                // halves BN*128 bytes apart).  The next S^T / dP^T overwrite P^T
-                // / dS^T only after these, in issue order.
                 gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_S, sdesc_sw128(sG(s), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
+                if (t + 1 < T) {
+                    if (!(ok = bounded_wait(bar(C::B_FULL + (t + 1) % NSTAGE),
+                                            ((t + 1) / NSTAGE) & 1, ctl)))
+                        break;
+                    issue_s(t + 1);
+                }
+                if (!(ok = bounded_wait(bar(C::B_DSRDY), t & 1, ctl))) break;
+                tc_fence_after();
                 gemm_ts_k8(tmem + C::TM_ACC1, tmem + C::TM_DP, sdesc_sw128(sQ(s), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
                 mma_commit(bar(C::B_EMPTY + s));
+                if (t + 1 < T) issue_dp(t + 1);
             }
             mma_commit(bar(C::B_DONE));
             drain_wait(bar(C::B_DONE), 0, timeout_ns);
@@ -295,10 +323,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(p[64 * h + 2 * i], p[64 * h + 2 * i + 1]);
                 tmem_st_32x32b_x32(tS + 32 * h, pk);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));  // dV += P^T dO may start
+            ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DPRDY), st & 1, ctl)) && ok;
+            tc_fence_after();
             ds_row(tDP, p, [&](int c) { return dv[c]; });
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
+            mbar_arrive(bar(C::B_DSRDY));
         }
         ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DONE), 0, ctl)) && ok;
         // K and V are no longer read (every MMA is done): stage dV and dK there.
@@ -366,7 +399,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(C::B_EMPTY + s), 1);
         }
         mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_DPRDY), 1);
         mbar_init(bar(C::B_PFULL), BM);
+        mbar_init(bar(C::B_DSRDY), BM);
         mbar_init(bar(C::B_DONE), 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -410,26 +445,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
             const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024), gdesc = sdesc_sw128(sG, 16, 1024);
-            bool ok = bounded_wait(bar(C::B_RES), 0, ctl);
+            // S = Q K^T and dP = dO V^T of key block t, each on its own barrier.
+            auto issue_s = [&](int t) {
+                const uint64_t b = sdesc_sw128(sK(t % NSTAGE), 16, 1024);
+                if constexpr (D == 128)
+                    gemm_ss_k8(tmem + C::TM_S, qdesc, b, idesc_s, 0u);
+                else
+                    gemm_ss_k4(tmem + C::TM_S, qdesc, b, idesc_s, 0u);
+                mma_commit(bar(C::B_SFULL));
+            };
+            auto issue_dp = [&](int t) {
+                const uint64_t b = sdesc_sw128(sV(t % NSTAGE), 16, 1024);
+                if constexpr (D == 128)
+                    gemm_ss_k8(tmem + C::TM_DP, gdesc, b, idesc_s, 0u);
+                else
+                    gemm_ss_k4(tmem + C::TM_DP, gdesc, b, idesc_s, 0u);
+                mma_commit(bar(C::B_DPRDY));
+            };
+            bool ok = bounded_wait(bar(C::B_RES), 0, ctl) && bounded_wait(bar(C::B_FULL), 0, ctl);
+            if (ok) {
+                issue_s(0);
+                issue_dp(0);
+            }
+            // Per block t: S of block t+1 as soon as the row warps have read S
+            // and block t+1 has landed (if it has not landed yet, after dQ),
+            // dQ += dS K (A = dS from TMEM, B = the K tile read MN-major), then
+            // dP of block t+1 (it overwrites dS, after dQ in issue order).
             for (int t = 0; ok && t < T; ++t) {
                 const int s = t % NSTAGE;
-                if (!(ok = bounded_wait(bar(C::B_FULL + s), (t / NSTAGE) & 1, ctl))) break;
-                // S = Q K^T and dP = dO V^T.
-                if constexpr (D == 128) {
-                    gemm_ss_k8(tmem + C::TM_S, qdesc, sdesc_sw128(sK(s), 16, 1024), idesc_s, 0u);
-                    gemm_ss_k8(tmem + C::TM_DP, gdesc, sdesc_sw128(sV(s), 16, 1024), idesc_s, 0u);
-                } else {
-                    gemm_ss_k4(tmem + C::TM_S, qdesc, sdesc_sw128(sK(s), 16, 1024), idesc_s, 0u);
-                    gemm_ss_k4(tmem + C::TM_DP, gdesc, sdesc_sw128(sV(s), 16, 1024), idesc_s, 0u);
+                bool s_next = false;
+                if (t + 1 < T) {
+                    if (!(ok = bounded_wait(bar(C::B_PFULL), t & 1, ctl))) break;  // S(t) read
+                    if (mbar_test_wait(bar(C::B_FULL + (t + 1) % NSTAGE), ((t + 1) / NSTAGE) & 1)) {
+                        issue_s(t + 1);
+                        s_next = true;
+                    }
                 }
-                mma_commit(bar(C::B_SFULL));
-                if (!(ok = bounded_wait(bar(C::B_PFULL), t & 1, ctl))) break;
+                if (!(ok = bounded_wait(bar(C::B_DSRDY), t & 1, ctl))) break;
                 tc_fence_after();
-                // dQ += dS K: A = dS (bf16 pairs in TMEM), B = the K tile read
-                // MN-major (keys along K, d contiguous).
                 gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_DP, sdesc_sw128(sK(s), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
                 mma_commit(bar(C::B_EMPTY + s));
+                if (t + 1 < T) {
+                    if (!s_next) {
+                        if (!(ok = bounded_wait(bar(C::B_FULL + (t + 1) % NSTAGE),
+                                                ((t + 1) / NSTAGE) & 1, ctl)))
+                            break;
+                        issue_s(t + 1);
+                    }
+                    issue_dp(t + 1);
+                }
             }
             mma_commit(bar(C::B_DONE));
             drain_wait(bar(C::B_DONE), 0, timeout_ns);
@@ -458,6 +523,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_ld_x32(r[1]);
             tmem_wait_ld_x32(r[2]);
             tmem_wait_ld_x32(r[3]);
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));  // S read: the next S may overwrite it
             const int key0 = st * BN;
             float p[128];
 #pragma unroll
@@ -465,10 +532,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float e = ex2_approx(fmaf(__uint_as_float(r[c >> 5][c & 31]), sl, nb));
                 p[c] = key0 + c < limit ? e : 0.f;
             }
+            ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DPRDY), st & 1, ctl)) && ok;
+            tc_fence_after();
             ds_row(tDP, p, [&](int) { return dl; });
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
+            mbar_arrive(bar(C::B_DSRDY));
         }
         ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DONE), 0, ctl)) && ok;
         // Q is no longer read: stage dQ there.
