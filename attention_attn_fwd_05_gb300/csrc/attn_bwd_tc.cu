@@ -115,12 +115,13 @@ __device__ __forceinline__ void stage_row(uint32_t tacc, uint32_t tile, int r, f
     }
 }
 
-// dS = P (dP - delta) for one row of 128 columns: P (fp32) is in p[]; dP is
-// read from TMEM 32 columns at a time and dS (bf16 pairs) written back over
-// the first 64 dP columns.  Chunk ch writes columns [16 ch, 16 ch + 16), all
-// of which belong to dP chunks already read.  `dl(c)` gives delta for column c.
-template <typename DeltaFn>
-__device__ __forceinline__ void ds_row(uint32_t tdp, const float (&p)[128], DeltaFn dl) {
+// dS = P (dP - D) for one row of 128 columns: P (fp32) is in p[]; dP is read
+// from TMEM 32 columns at a time and dS (bf16 pairs) written back over the
+// first 64 dP columns.  Chunk ch writes columns [16 ch, 16 ch + 16), all of
+// which belong to dP chunks already read.  `ndl(c)` gives the packed pair
+// (-D_c, -D_{c+1}); the arithmetic is packed (f32x2).
+template <typename NegDeltaFn>
+__device__ __forceinline__ void ds_row(uint32_t tdp, const float (&p)[128], NegDeltaFn ndl) {
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
         uint32_t g[32];
@@ -130,11 +131,45 @@ __device__ __forceinline__ void ds_row(uint32_t tdp, const float (&p)[128], Delt
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int c = 32 * ch + 2 * i;
-            const float d0 = p[c] * (__uint_as_float(g[2 * i]) - dl(c));
-            const float d1 = p[c + 1] * (__uint_as_float(g[2 * i + 1]) - dl(c + 1));
+            const uint64_t diff =
+                fadd2(pack_f32x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1])), ndl(c));
+            float d0, d1;
+            unpack_f32x2(fmul2(pack_f32x2(p[c], p[c + 1]), diff), d0, d1);
             pk[i] = pack_bf16x2(d0, d1);
         }
         tmem_st_32x32b_x16(tdp + 16 * ch, pk);
+    }
+}
+
+// P for one row of 128 columns: p[c] = 2^(s_c * sl + nb(c)), with nb(c) the
+// packed pair of biases for columns c, c+1; columns c < first_col are zero.
+// The mask is applied only where a block needs it.
+template <typename BiasFn>
+__device__ __forceinline__ void p_row(const uint32_t (&r)[4][32], float sl, BiasFn nb, int first_col,
+                                      int last_col, bool masked, float (&p)[128]) {
+    const uint64_t sl2 = pack_f32x2(sl, sl);
+    if (!masked) {
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+            float a0, a1;
+            unpack_f32x2(ffma2(pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
+                                          __uint_as_float(r[c >> 5][(c & 31) + 1])),
+                               sl2, nb(c)),
+                         a0, a1);
+            p[c] = ex2_approx(a0);
+            p[c + 1] = ex2_approx(a1);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+            float a0, a1;
+            unpack_f32x2(ffma2(pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
+                                          __uint_as_float(r[c >> 5][(c & 31) + 1])),
+                               sl2, nb(c)),
+                         a0, a1);
+            p[c] = (c >= first_col && c < last_col) ? ex2_approx(a0) : 0.f;
+            p[c + 1] = (c + 1 >= first_col && c + 1 < last_col) ? ex2_approx(a1) : 0.f;
+        }
     }
 }
 
@@ -292,10 +327,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int st = 0; st < T; ++st) {
             const int qb = q0 + st;
             float *nb = vec + (st & 1) * 2 * BN;  // -LSE log2e per query column
-            float *dv = nb + BN;                 // D per query column
+            float *dv = nb + BN;                 // -D per query column
             const int qi = qb * BN + t;
             nb[t] = qi < N ? -lse_bh[qi] * LOG2E : -INFINITY;  // rows past N: P = 0
-            dv[t] = qi < N ? dl_bh[qi] : 0.f;
+            dv[t] = qi < N ? -dl_bh[qi] : 0.f;  // -D, for the packed dP - D
             named_bar_sync(1, BM);
             ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL), st & 1, ctl)) && ok;
             tc_fence_after();
@@ -308,14 +343,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_ld_x32(r[1]);
             tmem_wait_ld_x32(r[2]);
             tmem_wait_ld_x32(r[3]);
-            // On the diagonal block, query column c sees this key only if c >= t.
-            const int first_col = (causal && qb == kb) ? t : 0;
+            // On the diagonal block, query column c sees this key only if c >= t
+            // (query rows past N already have a -inf bias).
+            const bool diag = causal && qb == kb;
             float p[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float e = ex2_approx(fmaf(__uint_as_float(r[c >> 5][c & 31]), sl, nb[c]));
-                p[c] = c >= first_col ? e : 0.f;
-            }
+            p_row(r, sl, [&](int c) { return *reinterpret_cast<const uint64_t *>(nb + c); },
+                  diag ? t : 0, 128, diag, p);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
@@ -328,7 +361,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(bar(C::B_PFULL));  // dV += P^T dO may start
             ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DPRDY), st & 1, ctl)) && ok;
             tc_fence_after();
-            ds_row(tDP, p, [&](int c) { return dv[c]; });
+            ds_row(tDP, p, [&](int c) { return *reinterpret_cast<const uint64_t *>(dv + c); });
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_DSRDY));
@@ -509,6 +542,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float sl = scale * LOG2E;
         const float nb = row < N ? -lse[(size_t)bh * N + row] * LOG2E : -INFINITY;
         const float dl = row < N ? delta[(size_t)bh * N + row] : 0.f;
+        const uint64_t nb2 = pack_f32x2(nb, nb), ndl2 = pack_f32x2(-dl, -dl);
         const int limit = causal ? min(N, row + 1) : N;  // keys [0, limit) are visible
         bool ok = true;
         for (int st = 0; st < T; ++st) {
@@ -525,16 +559,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_ld_x32(r[3]);
             tc_fence_before();
             mbar_arrive(bar(C::B_PFULL));  // S read: the next S may overwrite it
+            // Key columns [0, limit - key0) are visible; only the diagonal block
+            // (causal) and the block holding key N-1 need the mask.
             const int key0 = st * BN;
+            const bool masked = key0 + BN > (causal ? min(N, qb * BM + 1) : N);
             float p[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float e = ex2_approx(fmaf(__uint_as_float(r[c >> 5][c & 31]), sl, nb));
-                p[c] = key0 + c < limit ? e : 0.f;
-            }
+            p_row(r, sl, [&](int) { return nb2; }, 0, limit - key0, masked, p);
             ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_DPRDY), st & 1, ctl)) && ok;
             tc_fence_after();
-            ds_row(tDP, p, [&](int) { return dl; });
+            ds_row(tDP, p, [&](int) { return ndl2; });
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_DSRDY));
