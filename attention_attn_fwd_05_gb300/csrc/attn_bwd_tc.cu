@@ -20,9 +20,12 @@
 //         P^T = exp2(S^T scale log2e - LSE log2e),  dS^T = P^T (dP^T - D)
 //                                                     (CUDA cores, bf16 -> TMEM)
 //         dV += P^T dO,  dK += dS^T Q                  (TS MMAs, A from TMEM)
+//       issued as dV(t), S^T(t+1), dK(t), dP^T(t+1), so the row warps' work
+//       on block t overlaps dP^T(t), dV(t) and S^T(t+1).
 //   bwd_dq_tc_kernel     one CTA per 128-query block (queries on the lanes).
 //       Q and dO stay; K and V blocks stream.  Per key block:
-//         S = Q K^T,  dP = dO V^T;  dS = P (dP - D);  dQ += dS K.
+//         S = Q K^T,  dP = dO V^T;  dS = P (dP - D);  dQ += dS K,
+//       with S of the next block issued as soon as the row warps have read S.
 //
 // S and dP are recomputed in the second kernel (7 GEMMs where a single pass
 // with atomic dQ updates would do 5) so that every output row has exactly one
@@ -317,7 +320,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int t = threadIdx.x;  // 0..127 == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + C::TM_S, tDP = tmem + lane_base + C::TM_DP;
-        const int key = kb * BM + t;
         const float sl = scale * LOG2E;
         const float *lse_bh = lse + (size_t)bh * (size_t)N;
         const float *dl_bh = delta + (size_t)bh * (size_t)N;
@@ -384,7 +386,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_store_commit();
             tma_store_wait_read();
         }
-        (void)key;
     }
     tc_fence_before();
     __syncthreads();
