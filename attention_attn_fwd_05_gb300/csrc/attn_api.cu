@@ -110,7 +110,8 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
     if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
     const int64_t BH = B * H;
-    if (dtype == ATTN_BF16 && (N > kMaxNBf16 || BH > INT32_MAX)) return ATTN_ERR_SHAPE;
+    if (dtype == ATTN_BF16 && (N > kMaxNBf16 || BH > INT32_MAX || BH * ((N + 255) / 256) > INT32_MAX))
+        return ATTN_ERR_SHAPE;
     if (dtype == ATTN_F32 && (BH > 65535 || (N + 31) / 32 > INT32_MAX)) return ATTN_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_ALIGN;

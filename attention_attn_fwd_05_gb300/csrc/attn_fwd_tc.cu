@@ -41,6 +41,14 @@
 //               the end O / l -> bf16 -> shared (the Q buffer of the tile, no
 //               longer read) -> TMA store, and LSE = (m + log2 l) ln 2.
 //
+// The launch is a list of items, one per (batch*head, 256-row query block),
+// batch*head fastest and heaviest causal blocks first, on a 1-D grid, so the
+// hardware's in-order dispatch acts as a longest-first schedule.  Items that
+// would leave a last wave at most half full (without the causal mask), or all
+// items of a grid that fills at most half the SMs, go to a second launch of
+// attn_fwd_bf16_tc_split_kernel: two CTAs per item, each on one 128-row half,
+// with tile A on the even and tile B on the odd key tiles (see there).
+//
 // The N x N logits live only in TMEM and registers; device memory sees Q, K,
 // V read and O, LSE written.
 #include <cuda.h>
@@ -82,9 +90,9 @@ struct Cfg {
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
     // Barrier slots (8 bytes each).
     static constexpr int B_Q = 0;     // [2] Q_A, Q_B landed
-    static constexpr int B_FULL = 2;
-    static constexpr int B_EMPTY = B_FULL + NSLOT;
-    static constexpr int B_SFULL = B_EMPTY + NSLOT;  // [2]
+    static constexpr int B_FULL = 2;                   // [NSLOT + 1] (the split kernel's ring
+    static constexpr int B_EMPTY = B_FULL + NSLOT + 1;  //  has one more slot)
+    static constexpr int B_SFULL = B_EMPTY + NSLOT + 1;  // [2]
     static constexpr int B_PFULL = B_SFULL + 2;      // [2]
     static constexpr int B_ODONE = B_PFULL + 2;      // [2]
     static constexpr int B_DRAIN = B_ODONE + 2;
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
                             const __grid_constant__ CUtensorMap tmO, float *__restrict__ lse,
-                            int N, int num_cta_tiles, float scale_log2, int causal,
+                            int N, int BH, int num_cta_tiles, float scale_log2, int causal,
                             uint32_t *status, uint64_t timeout_ns, int num_sms) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -296,9 +304,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    // Heaviest causal tiles first: grid.y walks CTA tiles from the end.
-    const int cta_tile = causal ? (num_cta_tiles - 1 - (int)blockIdx.y) : (int)blockIdx.y;
+    // Items in launch order: batch*head fastest, heaviest causal tiles first.
+    const int bh = (int)blockIdx.x % BH;
+    const int cta_tile =
+        causal ? (num_cta_tiles - 1 - (int)blockIdx.x / BH) : (int)blockIdx.x / BH;
     const int row0 = cta_tile * (2 * BM);
     int TA, TB;
     tile_counts(N, cta_tile, causal, TA, TB);
@@ -341,9 +350,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Warm L2 with the query block of the CTA that will most likely start
         // next on a free SM (blocks are dispatched in launch order, so that is
         // the one num_sms further on).
-        const int next = ((int)blockIdx.y * (int)gridDim.x + (int)blockIdx.x) + num_sms;
-        if (next < (int)(gridDim.x * gridDim.y)) {
-            const int nbh = next % (int)gridDim.x, ny = next / (int)gridDim.x;
+        const int next = (int)blockIdx.x + num_sms;
+        if (next < (int)gridDim.x) {
+            const int nbh = next % BH, ny = next / BH;
             const int ntile = causal ? (num_cta_tiles - 1 - ny) : ny;
             for (int x = 0; x < 2; ++x) {
                 const int r = ntile * (2 * BM) + x * BM;
@@ -465,6 +474,355 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ------------------------------------------------------ split CTAs ---
+//
+// For the items of a last, partly filled wave (without the causal mask), or
+// for every item of a grid that fills at most half the SMs, two CTAs share an
+// item, one per 128-row half.  In such a CTA both query tiles hold the same
+// rows (Q is loaded once, into Q_A): tile A walks the even key tiles and tile
+// B the odd ones, with the same MMA order as the main kernel (S_A(j),
+// O_B += P_B(j-1) V, S_B(j), O_A += P_A(j) V), so the tensor core still works
+// on one tile while the other's softmax runs.  At the end the two partial
+// results (m, l, O) of each row are merged with the online rule.  Every step
+// streams two K and two V tiles, so the ring gets one more slot: the unused
+// Q_B buffer.
+
+// Ring entries of step j: tile x takes key tile 2j + x, whose K is entry
+// 2(2j + x) and V the next one.
+__device__ __forceinline__ int split_entry_k(int x, int j) { return 4 * j + 2 * x; }
+
+template <int D>
+__device__ __forceinline__ uint32_t split_slot_addr(uint32_t sbase, int n) {
+    using C = Cfg<D>;
+    const int s = n % (C::NSLOT + 1);
+    return s < C::NSLOT ? sbase + C::OFF_KV + (uint32_t)s * C::SLOT_BYTES
+                        : sbase + C::OFF_Q + C::Q_BYTES;
+}
+
+template <int D>
+__device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t tmem, uint32_t sbase,
+                                              float *xch, int T, int TB, int row0, int N,
+                                              int causal, float scale_log2,
+                                              float *__restrict__ lse, int bh,
+                                              const CUtensorMap *tmO, const WaitCtl &ctl,
+                                              volatile uint32_t *abort_flag) {
+    using C = Cfg<D>;
+    constexpr int NS = C::NSLOT + 1;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (x ? C::TM_S1 : C::TM_S0);
+    const uint32_t tO = tmem + lane_base + (x ? C::TM_O1 : C::TM_O0);
+    const int row = row0 + t;
+    const int limit = causal ? min(N, row + 1) : N;
+    const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+        ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL + x), j & 1, ctl));
+        if (!ok) break;
+        if (t == 0) {
+            // S_x(j) is complete, and with it every MMA issued before it: its
+            // own K tile is free, and so is the V tile this tile read in the
+            // previous step (O_x += P_x(j-1) V was issued before S_x(j)).
+            const int e = split_entry_k(x, j);
+            mbar_arrive(bar(C::B_EMPTY + e % NS));
+            if (j >= 1) mbar_arrive(bar(C::B_EMPTY + (e - 3) % NS));
+        }
+        tc_fence_after();
+        uint32_t r[4][32];
+        tmem_ld_32x32b_x32(tS + 0, r[0]);
+        tmem_ld_32x32b_x32(tS + 32, r[1]);
+        tmem_ld_32x32b_x32(tS + 64, r[2]);
+        tmem_ld_32x32b_x32(tS + 96, r[3]);
+        tmem_wait_ld_x32(r[0]);
+        tmem_wait_ld_x32(r[1]);
+        tmem_wait_ld_x32(r[2]);
+        tmem_wait_ld_x32(r[3]);
+        const int key0 = (2 * j + x) * BN;
+        if (key0 + BN > limit) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+                if (key0 + c >= limit) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i >> 1][(i & 1) * 16]);
+#pragma unroll
+        for (int c = 1; c < 16; c += 2) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int base = (i & 1) * 16;
+                mx8[i] = fmax3(mx8[i], __uint_as_float(r[i >> 1][base + c]),
+                               __uint_as_float(r[i >> 1][base + (c + 1 < 16 ? c + 1 : c)]));
+            }
+        }
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        const float m_new = mx * scale_log2;
+        const bool upd = m_new > m_ref + RESCALE_THRESHOLD;
+        float m_use = upd ? m_new : m_ref;
+        if (m_use == -INFINITY) m_use = 0.f;
+        const float alpha = upd ? ex2_approx(m_ref - m_use) : 1.f;
+        const uint64_t neg_m = pack_f32x2(-m_use, -m_use);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+            const uint64_t sv = pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
+                                           __uint_as_float(r[c >> 5][(c & 31) + 1]));
+            float a0, a1;
+            unpack_f32x2(ffma2(sv, scale2, neg_m), a0, a1);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pack_f32x2(p0, p1));
+            pk[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_32x32b_x32(tS + 0, pk[0]);
+        tmem_st_32x32b_x32(tS + 32, pk[1]);
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        unpack_f32x2(acc[0], s0, s1);
+        unpack_f32x2(acc[1], s2, s3);
+        unpack_f32x2(acc[2], s4, s5);
+        unpack_f32x2(acc[3], s6, s7);
+        const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        if (j > 0 && __any_sync(0xffffffffu, upd)) {
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tO + c, o);
+                tmem_wait_ld_x32(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st_32x32b_x32(tO + c, o);
+            }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PFULL + x));
+        l_run = l_run * alpha + rs;
+        m_ref = m_use;
+    }
+    // Merge.  The exchange area is a ring slot (Q_B), which the other tile's
+    // last O += P V may still be reading: both tiles wait until every MMA of
+    // the CTA is done (tile B has none when the rows see only one key tile).
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + 0), 0, ctl));
+    if (ok && TB > 0) ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + 1), 0, ctl));
+    xch[(2 * x) * BM + t] = T > 0 ? m_ref : -INFINITY;
+    xch[(2 * x + 1) * BM + t] = l_run;
+    named_bar_sync(3, 2 * BM);
+    const float mA = xch[t], lA = xch[BM + t], mB = xch[2 * BM + t], lB = xch[3 * BM + t];
+    const float m = fmaxf(mA, mB);
+    const float a = ex2_approx(mA - m);
+    const float b = TB > 0 ? ex2_approx(mB - m) : 0.f;
+    const float l = a * lA + b * lB;
+    if (ok) {
+        tc_fence_after();
+        const float ia = a / l, ib = b / l;
+        const uint32_t sOut = sbase + C::OFF_Q;  // Q_A: no MMA reads it any more
+        const uint32_t tOA = tmem + lane_base + C::TM_O0, tOB = tmem + lane_base + C::TM_O1;
+        // Tile A's threads merge columns [0, D/2), tile B's [D/2, D).
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            const int c = x * (D / 2) + c0;
+            uint32_t oa[32], ob[32];
+            tmem_ld_32x32b_x32(tOA + c, oa);
+            tmem_wait_ld_x32(oa);
+            if (TB > 0) {
+                tmem_ld_32x32b_x32(tOB + c, ob);
+                tmem_wait_ld_x32(ob);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ob[i] = 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int dcol = c + i * 8;
+                const uint32_t chunk = (uint32_t)(dcol & 63) >> 3;
+                const uint32_t addr = sOut + (dcol >> 6) * (BM * 128) + t * 128 +
+                                      ((chunk ^ ((uint32_t)t & 7u)) << 4);
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] = __uint_as_float(oa[i * 8 + e]) * ia + __uint_as_float(ob[i * 8 + e]) * ib;
+                st_shared_v4(addr, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            }
+        }
+        if (x == 0 && lse != nullptr && row < N)
+            lse[(size_t)bh * (size_t)N + (size_t)row] = (m + log2f(l)) * LN2;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(3, 2 * BM);
+    if (x == 0 && t == 0 && ok && *abort_flag == 0u) {
+        for (int c = 0; c < C::DBLK; ++c)
+            tma_store_3d(tmO, sbase + C::OFF_Q + c * (BM * 128), c * 64, row0, bh);
+        tma_store_commit();
+        tma_store_wait_read();
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_bf16_tc_split_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                  const __grid_constant__ CUtensorMap tmK,
+                                  const __grid_constant__ CUtensorMap tmV,
+                                  const __grid_constant__ CUtensorMap tmO,
+                                  float *__restrict__ lse, int N, int BH, int num_cta_tiles,
+                                  int first_item, float scale_log2, int causal, uint32_t *status,
+                                  uint64_t timeout_ns) {
+    using C = Cfg<D>;
+    constexpr int NS = C::NSLOT + 1;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::OFF_Q;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM_SLOT);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_ABORT);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // CTA 2i + h takes the 128-row half h of item first_item + i.
+    const int item = first_item + (int)(blockIdx.x >> 1);
+    const int bh = item % BH;
+    const int rank = item / BH;
+    const int cta_tile = causal ? (num_cta_tiles - 1 - rank) : rank;
+    const int row0 = cta_tile * (2 * BM) + (int)(blockIdx.x & 1) * BM;
+    if (row0 >= N) return;  // rows past N: nothing to do (uniform, before any setup)
+    const int nkv = (N + BN - 1) / BN;
+    const int KT = causal ? min(row0 / BM + 1, nkv) : nkv;  // key tiles these rows see
+    const int TA = (KT + 1) >> 1, TB = KT >> 1;              // even / odd key tiles
+
+    auto load_kv = [&](int n) {  // entry n: K (even n) or V (odd n) of key tile n / 2
+        const int s = n % NS;
+        mbar_arrive_expect_tx(bar(C::B_FULL + s), C::SLOT_BYTES);
+        const uint32_t dst = split_slot_addr<D>(sbase, n);
+        for (int c = 0; c < C::DBLK; ++c)
+            tma_load_3d(dst + c * (BN * 128), (n & 1) ? &tmV : &tmK, c * 64, (n >> 1) * BN, bh,
+                        bar(C::B_FULL + s));
+    };
+    if (warp == WARP_TMA && lane == 0) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(C::B_Q + x), 1);
+            mbar_init(bar(C::B_SFULL + x), 1);
+            mbar_init(bar(C::B_PFULL + x), BM);
+            mbar_init(bar(C::B_ODONE + x), 1);
+        }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_DRAIN), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar(C::B_Q), C::Q_BYTES);
+        for (int c = 0; c < C::DBLK; ++c)
+            tma_load_3d(sQ + c * (BM * 128), &tmQ, c * 64, row0, bh, bar(C::B_Q));
+        load_kv(0);
+        load_kv(1);
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, status, timeout_ns};
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            const int n_loads = 2 * KT;
+            int n = 2;
+            for (; n < n_loads; ++n) {
+                const int s = n % NS;
+                if (n >= NS && !bounded_wait(bar(C::B_EMPTY + s), ((n / NS) - 1) & 1, ctl)) break;
+                load_kv(n);
+            }
+            drain_wait(bar(C::B_Q), 0, timeout_ns);
+            for (int i = (n > NS ? n - NS : 0); i < n; ++i)
+                drain_wait(bar(C::B_FULL + i % NS), (i / NS) & 1, timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
+            auto wait_full = [&](int n) -> bool {
+                return bounded_wait(bar(C::B_FULL + n % NS), (n / NS) & 1, ctl);
+            };
+            const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);  // both tiles read Q_A
+            auto issue_s = [&](int x, int n) {
+                const uint32_t dS = tmem + (x ? C::TM_S1 : C::TM_S0);
+                const uint64_t kd = sdesc_sw128(split_slot_addr<D>(sbase, n), 16, 1024);
+                if constexpr (D == 128)
+                    gemm_ss_k8(dS, qdesc, kd, idesc_s, 0u);
+                else
+                    gemm_ss_k4(dS, qdesc, kd, idesc_s, 0u);
+                mma_commit(bar(C::B_SFULL + x));
+            };
+            auto issue_pv = [&](int x, int n, bool first) {
+                gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + (x ? C::TM_S1 : C::TM_S0),
+                           sdesc_sw128(split_slot_addr<D>(sbase, n), BN * 128, 1024), idesc_o,
+                           first ? 0u : 1u);
+            };
+            bool ok = bounded_wait(bar(C::B_Q), 0, ctl);
+            for (int j = 0; ok && j < TA; ++j) {  // TA >= TB
+                const int nKA = split_entry_k(0, j), nKB = split_entry_k(1, j);
+                if (!(ok = wait_full(nKA))) break;
+                issue_s(0, nKA);
+                if (j >= 1) {
+                    // O_B += P_B(j-1) V (key tile 2j - 1).
+                    const int nV = split_entry_k(1, j - 1) + 1;
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl) &&
+                               wait_full(nV)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(1, nV, j == 1);
+                    if (j - 1 == TB - 1) mma_commit(bar(C::B_ODONE + 1));
+                }
+                if (j < TB) {
+                    if (!(ok = wait_full(nKB))) break;
+                    issue_s(1, nKB);
+                }
+                const int nV = nKA + 1;
+                if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl) && wait_full(nV))) break;
+                tc_fence_after();
+                issue_pv(0, nV, j == 0);
+                if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
+            }
+            if (ok && TB >= 1 && TA == TB) {
+                const int j = TB - 1, nV = split_entry_k(1, j) + 1;
+                ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl) && wait_full(nV);
+                if (ok) {
+                    tc_fence_after();
+                    issue_pv(1, nV, j == 0);
+                    mma_commit(bar(C::B_ODONE + 1));
+                }
+            }
+            mma_commit(bar(C::B_DRAIN));
+            drain_wait(bar(C::B_DRAIN), 0, timeout_ns);
+        }
+        __syncwarp();
+    } else {
+        const int x = warp >> 2;
+        const int t = threadIdx.x & 127;
+        // The merge exchanges (m, l) through the start of Q_B, which no MMA
+        // reads by then.
+        split_softmax<D>(x, t, warp, tmem, sbase,
+                         reinterpret_cast<float *>(smem + C::OFF_Q + C::Q_BYTES), x ? TB : TA, TB,
+                         row0, N, causal, scale_log2, lse, bh, &tmO, ctl, abort_flag);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 // A kernel whose only job is to wait, through bounded_wait, on a barrier that
 // nothing signals: exercises the timeout path without hanging the GPU.
 __global__ void wait_selftest_kernel(uint32_t *status, uint64_t timeout_ns) {
@@ -535,13 +893,44 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
                                           (int)C::SMEM_BYTES),
                      ATTN_ERR_CUDA) != ATTN_OK)
         return ATTN_ERR_CUDA;
+    if (check_launch(cudaFuncSetAttribute(attn_fwd_bf16_tc_split_kernel<D>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)C::SMEM_BYTES),
+                     ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
     const int num_cta_tiles = (int)((N + 2 * BM - 1) / (2 * BM));
+    const int64_t n_items = BH * num_cta_tiles;
+    // Items taken by two split CTAs (one per 128-row half): all of them when
+    // they fill at most half the SMs; without the causal mask, also the items
+    // that would otherwise run in a last wave filling at most half the SMs.
+    // Those go to a second launch, after whole waves of the main kernel.
+    // (With the mask the last items are the lightest: no split.)
+    const int64_t sms = ctx.sm_count > 0 ? ctx.sm_count : 1;
+    int64_t n_split = 0;
+    if (2 * n_items <= sms) {
+        n_split = n_items;
+    } else if (!causal) {
+        const int64_t rem = n_items % sms;
+        if (rem > 0 && 2 * rem <= sms) n_split = rem;
+    }
+    const int64_t n_main = n_items - n_split;
     const float scale_log2 = scale * 1.44269504088896340736f;
-    dim3 grid((unsigned)BH, (unsigned)num_cta_tiles);
-    attn_fwd_bf16_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
-        tq, tk, tv, to, lse, (int)N, num_cta_tiles, scale_log2, causal ? 1 : 0, ctx.status,
-        ctx.timeout_ns, ctx.sm_count);
-    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+    if (n_main > 0) {
+        attn_fwd_bf16_tc_kernel<D><<<(unsigned)n_main, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
+            tq, tk, tv, to, lse, (int)N, (int)BH, num_cta_tiles, scale_log2, causal ? 1 : 0,
+            ctx.status, ctx.timeout_ns, ctx.sm_count);
+        const attn_status st = check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+        if (st != ATTN_OK) return st;
+    }
+    if (n_split > 0) {
+        attn_fwd_bf16_tc_split_kernel<D><<<(unsigned)(2 * n_split), NUM_THREADS, C::SMEM_BYTES,
+                                           ctx.stream>>>(tq, tk, tv, to, lse, (int)N, (int)BH,
+                                                         num_cta_tiles, (int)n_main, scale_log2,
+                                                         causal ? 1 : 0, ctx.status,
+                                                         ctx.timeout_ns);
+        return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+    }
+    return ATTN_OK;
 }
 
 }  // namespace tc

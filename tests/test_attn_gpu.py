@@ -75,6 +75,26 @@ def test_parity_small(dtype, d, causal, B, H, N):
                  f"{dtype} d={d} causal={causal} {B}x{H}x{N}")
 
 
+# Small grids (at most half as many 256-row items as SMs) run entirely on the
+# split kernel (two CTAs per item, key tiles split between the two query
+# tiles), so the shapes above exercise it.  These shapes have more items than
+# that: the main kernel runs, and without the causal mask the items of a last
+# wave that would be at most half full go to the split kernel after it.
+MIXED_SHAPES = [(2, 40, 300), (1, 80, 129), (1, 160, 40)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", MIXED_SHAPES)
+def test_parity_main_kernel_and_tail(d, causal, B, H, N):
+    q, k, v = make_qkv(B, H, N, d, seed=2000 + N + d + H, dtype="bf16")
+    scale = _scale(d)
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    assert_close("bf16", o, lse, o_ref, lse_ref, float(v.float().abs().max()),
+                 f"bf16 d={d} causal={causal} {B}x{H}x{N}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_parity_stress_logits_small(causal):
     """Large logits (variance-16 Q and K) on a ragged size: online-softmax stability."""
