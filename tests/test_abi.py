@@ -68,6 +68,12 @@ def test_bf16_sequence_limit(L):
     assert call(L, N=65535 * 128 + 1) == 2
 
 
+def test_bf16_grid_limit(L):
+    """B*H*ceil(N/256) items must fit the kernels' 1-D grid (< 2^31)."""
+    assert call(L, B=1024, H=128, N=65535 * 128) == 2
+    assert call(L, B=1024, H=128, N=65535 * 128, dtype=0) == 2  # and fp32: B*H > 65535
+
+
 def test_f32_head_limit(L):
     assert call(L, B=65536, H=1, N=1, dtype=0) == 2
 
