@@ -213,6 +213,73 @@ def config_of(w):
             if io > 2 * L2_BYTES else "L2 flushed (256 MB write) before each timed step"}
 
 
+def launches_per_call(w, sms: int) -> int:
+    """Kernels one attn_fwd call launches.  bf16: the main kernel plus, when
+    some items go to split CTAs (all items of a grid filling at most half the
+    SMs; without the causal mask, also a last wave filling at most half of
+    them), the split-CTA kernel.  fp32: one kernel."""
+    if w.dtype != "bf16":
+        return 1
+    n_items = w.B * w.H * ((w.N + 255) // 256)
+    if 2 * n_items <= sms:
+        n_split = n_items
+    elif not w.causal and 0 < n_items % sms and 2 * (n_items % sms) <= sms:
+        n_split = n_items % sms
+    else:
+        n_split = 0
+    return int(n_items - n_split > 0) + int(n_split > 0)
+
+
+EAGER_MAX_SCORE_BYTES = 8 << 30
+
+
+def eager_context(w, qd, kd, vd, our_ms: float, our_extra: int, dev, reps: int = 5):
+    """The pages' own baseline re-run on this GPU, as context only: PyTorch
+    eager fp32 softmax(scale * Q K^T) V with S and P materialised (inputs
+    upcast to fp32, no TF32), timed with CUDA events, and the device memory it
+    takes beyond its inputs.  Not part of `value` and never a fallback."""
+    scores = w.B * w.H * w.N * w.N * 4
+    if scores > EAGER_MAX_SCORE_BYTES:
+        return {"skipped": f"S and P would need {2 * scores / 2**30:.1f} GiB"}
+    q32, k32, v32 = (t.float() for t in (qd, kd, vd))
+    mask = torch.ones(w.N, w.N, dtype=torch.bool, device=dev).triu_(1) if w.causal else None
+
+    def run():
+        s_ = torch.matmul(q32, k32.transpose(-1, -2)) * w.scale
+        if mask is not None:
+            s_ = s_.masked_fill(mask, float("-inf"))
+        return torch.matmul(torch.softmax(s_, dim=-1), v32)
+
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        run()
+        torch.cuda.synchronize(dev)
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        out = run()
+        torch.cuda.synchronize(dev)
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        del out
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+    eager_ms = statistics.median(times)
+    ours_bytes = w.B * w.H * w.N * (w.d * (2 if w.dtype == "bf16" else 4) + 4) + our_extra
+    return {"kind": "context: PyTorch eager fp32 on this GPU (the pages' baseline)",
+            "ms": eager_ms, "speedup_of_ours": eager_ms / our_ms,
+            "eager_peak_bytes_beyond_inputs": peak,
+            "ours_bytes_beyond_inputs": ours_bytes,
+            "memory_reduction": 1.0 - ours_bytes / peak if peak > 0 else None}
+
+
 def run_ours(args, w):
     from attention_attn_fwd_05_gb300 import attn_fwd, attn_fwd_host, device_status
     world, rank, local = dist_env()
@@ -342,11 +409,14 @@ def run_ours(args, w):
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call(
+            w, torch.cuda.get_device_properties(dev).multi_processor_count),
         "clocks": clk.summary(),
         "memory": memory,
         "gpu": torch.cuda.get_device_name(dev),
     }
+    if args.context_eager:
+        line["context_eager"] = eager_context(w, qd, kd, vd, step_ms, extra, dev)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -475,6 +545,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--context-eager", action="store_true",
+                    help="also time PyTorch eager fp32 attention on the GPU (context only)")
     ap.add_argument("--op", default="attn",
                     choices=["attn", "attn_bwd", "row_softmax", "add_rmsnorm"],
                     help="attn (the hot path, default) or one of the HBM-bound kernels")
