@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "attn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attn {
 namespace rms {
@@ -146,12 +147,150 @@ __global__ void __launch_bounds__(NT)
     }
 }
 
+// ------------------------------------------------------------------ streamed ---
+// The register-resident path with its input rows streamed: each CTA copies
+// the x (and residual) rows of its next row into the other of two
+// shared-memory stages with bulk async copies while it works on the current
+// one, so reads stay in flight through the row's reduction and stores.
+
+constexpr uint32_t ST_HDR = 256;  // two barriers, abort flag, reduction scratch
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ void load8s(const uint8_t *p, float (&v)[8]) {
+    load8(reinterpret_cast<const T *>(p), v);
+}
+
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(NT)
+    add_rmsnorm_stream_kernel(const T *__restrict__ x, const T *__restrict__ res,
+                              const T *__restrict__ w, T *__restrict__ out,
+                              T *__restrict__ res_out, int64_t rows, int width, float eps,
+                              uint32_t *status, uint64_t timeout_ns) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const uint32_t sbase = smem_u32(sm);  // barrier of stage s at sbase + 8s
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + 64);
+    float *red = reinterpret_cast<float *>(sm + 96);  // [NT / 32 + 1]
+    const bool has_res = res != nullptr;
+    const uint32_t row_bytes = (uint32_t)width * (uint32_t)sizeof(T);
+    const uint32_t stride = (row_bytes + 127u) & ~127u;
+    const uint32_t stage_bytes = (has_res ? 2u : 1u) * stride;
+    const int nvec = width / VEC;
+    const WaitCtl ctl{abort_flag, status, timeout_ns};
+    const int64_t G = gridDim.x;
+    int n_issued = 0;  // rows of this CTA whose copies thread 0 started
+    auto issue = [&]() {
+        const int64_t row = (int64_t)blockIdx.x + (int64_t)n_issued * G;
+        if (row >= rows) return;
+        const uint32_t s = (uint32_t)(n_issued & 1), bar = sbase + 8u * s;
+        const uint32_t dst = sbase + ST_HDR + s * stage_bytes;
+        mbar_arrive_expect_tx(bar, (has_res ? 2u : 1u) * row_bytes);
+        bulk_copy_g2s(dst, x + row * (int64_t)width, row_bytes, bar);
+        if (has_res) bulk_copy_g2s(dst + stride, res + row * (int64_t)width, row_bytes, bar);
+        ++n_issued;
+    };
+    if (threadIdx.x == 0) {
+        mbar_init(sbase, 1);
+        mbar_init(sbase + 8, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        issue();
+        issue();
+    }
+    __syncthreads();
+
+    int i = 0;
+    for (int64_t r = blockIdx.x; r < rows; ++i, r += G) {
+        const uint32_t s = (uint32_t)(i & 1);
+        if (!__syncthreads_and(
+                bounded_wait_warp(sbase + 8u * s, (uint32_t)(i >> 1) & 1u, ctl) ? 1 : 0))
+            break;
+        const uint8_t *sx = sm + ST_HDR + s * stage_bytes;
+        float h[KMAX][VEC];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            const int vi = threadIdx.x + k * NT;
+            if (vi < nvec) {
+                load8s<T>(sx + (uint32_t)vi * VEC * sizeof(T), h[k]);
+                if (has_res) {
+                    float b[VEC];
+                    load8s<T>(sx + stride + (uint32_t)vi * VEC * sizeof(T), b);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) h[k][e] += b[e];
+                }
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) ss = fmaf(h[k][e], h[k][e], ss);
+            }
+        }
+        // block_sum's barriers also mean every thread is done with stage s.
+        const float inv = 1.f / sqrtf(block_sum(ss, red) / (float)width + eps);
+        if (threadIdx.x == 0) issue();  // row i + 2 into stage s
+        T *orow = out + r * (int64_t)width;
+        T *hrow = has_res ? res_out + r * (int64_t)width : nullptr;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            const int vi = threadIdx.x + k * NT;
+            if (vi < nvec) {
+                if (has_res) store8(hrow + vi * VEC, h[k]);
+                float g[VEC];
+                load8(w + vi * VEC, g);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) h[k][e] = h[k][e] * inv * g[e];
+                store8(orow + vi * VEC, h[k]);
+            }
+        }
+    }
+    // After a timeout, let copies still in flight land before the CTA exits.
+    if (threadIdx.x == 0 && *abort_flag != 0u) {
+        for (int c = i; c < n_issued; ++c) {
+            const uint32_t bar = sbase + 8u * (uint32_t)(c & 1);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar, (uint32_t)(c >> 1) & 1u))
+                if (globaltimer_ns() - t0 > timeout_ns) break;
+        }
+    }
+}
+
+template <typename T>
+static attn_status launch_stream(const T *x, const T *residual, const T *weight, T *out,
+                                 T *res_out, int64_t rows, int width, float eps,
+                                 const LaunchCtx &ctx) {
+    const uint32_t stride = ((uint32_t)width * (uint32_t)sizeof(T) + 127u) & ~127u;
+    const int smem = (int)(ST_HDR + 2u * (residual ? 2u : 1u) * stride);
+    auto kern = add_rmsnorm_stream_kernel<T, MAXV>;
+    if (check_launch(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                     ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    int per_sm = 0;
+    if (check_launch(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem),
+                     ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    const int64_t max_grid = (int64_t)ctx.sm_count * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = (unsigned)(rows < max_grid ? rows : max_grid);
+    kern<<<grid, NT, smem, ctx.stream>>>(x, residual, weight, out, res_out, rows, width, eps,
+                                         ctx.status, ctx.timeout_ns);
+    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+}
+
 }  // namespace rms
 
 attn_status launch_add_rmsnorm(const void *x, const void *residual, const void *weight, void *out,
                                void *res_out, int64_t rows, int64_t width, float eps, int dtype,
                                const LaunchCtx &ctx) {
     const int fast = (width % rms::VEC == 0 && width <= rms::MAX_FAST) ? 1 : 0;
+    if (fast && dtype != ATTN_F32)
+        return rms::launch_stream<uint16_t>(
+            static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(residual),
+            static_cast<const uint16_t *>(weight), static_cast<uint16_t *>(out),
+            static_cast<uint16_t *>(res_out), rows, (int)width, eps, ctx);
     const int64_t max_grid = (int64_t)ctx.sm_count * 8;
     const unsigned grid = (unsigned)(rows < max_grid ? rows : max_grid);
     if (dtype == ATTN_F32) {

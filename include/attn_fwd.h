@@ -123,6 +123,8 @@ attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v, void *
  *   y     [rows, width] fp32 output (device, fully overwritten), may equal x.
  *   lse   [rows] fp32 natural-log log-sum-exp per row, or NULL.
  *   rows, width >= 1, rows*width < 2^62.  Any width is accepted.
+ *   -inf entries get probability 0; a row of -inf only gets all zeros and
+ *   LSE = -inf.
  * Returns ATTN_OK or a validation / launch error (as attn_fwd).
  */
 attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,

@@ -48,8 +48,12 @@ def test_bounded_wait_times_out_and_context_survives():
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
 
 
+# Widths that are multiples of 4 up to 12288 take the streamed kernel (many
+# rows per CTA cycle through its 2-8 buffers and their phases); the others the
+# general one.
 @pytest.mark.parametrize("rows,width", [(1, 1), (3, 5), (64, 1000), (8, 11264), (4, 11265),
-                                        (2, 70000), (300, 4096)])
+                                        (2, 70000), (3000, 4096), (12000, 1024), (700, 12288),
+                                        (2500, 8192), (50, 12292), (9000, 4)])
 def test_row_softmax_parity(rows, width):
     """Row softmax (any width, including rows past 65536) against the oracle."""
     x = make_rows(rows, width, seed=rows + width, spread=6.0)
@@ -61,6 +65,38 @@ def test_row_softmax_parity(rows, width):
     assert np.all(np.abs(yd - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-5 * max(1.0, np.abs(lse_ref).max())
     np.testing.assert_allclose(yd.sum(axis=1), 1.0, rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("rows,width", [(5, 513), (5000, 512)])
+def test_row_softmax_masked_and_in_place_both_paths(rows, width):
+    """-inf entries get probability 0, in place, on either kernel."""
+    x = make_rows(rows, width, seed=rows + 3, spread=3.0)
+    x[:, ::7] = float("-inf")
+    y_ref, _ = oracle.row_softmax(torch.where(torch.isinf(x), torch.full_like(x, -1e30), x))
+    xd = x.cuda()
+    row_softmax(xd, out=xd)
+    torch.cuda.synchronize()
+    yd = xd.cpu().numpy().astype(np.float64)
+    assert (yd[:, ::7] == 0).all()
+    assert np.all(np.abs(yd - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)
+
+
+@pytest.mark.parametrize("width", [513, 512])
+def test_row_softmax_fully_masked_row(width):
+    """A row of -inf only: every probability 0 and LSE = -inf; other rows unaffected."""
+    n = 3000
+    x = make_rows(n, width, seed=width, spread=3.0)
+    x[7] = float("-inf")
+    x[n - 1] = float("-inf")
+    y, lse = row_softmax(x.cuda(), return_lse=True)
+    torch.cuda.synchronize()
+    yd, ld = y.cpu().numpy().astype(np.float64), lse.cpu().numpy()
+    assert (yd[7] == 0).all() and (yd[n - 1] == 0).all()
+    assert np.isneginf(ld[7]) and np.isneginf(ld[n - 1])
+    keep = [i for i in range(n) if i not in (7, n - 1)]
+    y_ref, lse_ref = oracle.row_softmax(x[keep])
+    assert np.all(np.abs(yd[keep] - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)
+    assert np.abs(ld[keep] - lse_ref).max() <= 1e-5 * max(1.0, np.abs(lse_ref).max())
 
 
 def test_row_softmax_masked_and_in_place():

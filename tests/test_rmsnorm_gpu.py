@@ -25,8 +25,11 @@ def _inputs(rows, width, dtype, seed):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("with_res", [False, True])
+# bf16 rows of up to 8192 elements (a multiple of 8) stream through two
+# shared-memory stages; the larger row counts make each CTA cycle through both.
 @pytest.mark.parametrize("rows,width", [(1, 1), (3, 7), (33, 8), (300, 100), (64, 512),
-                                        (16, 4096), (8, 8192), (5, 8200), (3, 20000)])
+                                        (16, 4096), (8, 8192), (5, 8200), (3, 20000),
+                                        (3000, 1024), (2000, 8192)])
 def test_add_rmsnorm_parity(dtype, with_res, rows, width):
     x, r, w = _inputs(rows, width, dtype, seed=rows * 31 + width)
     eps = 1e-6
