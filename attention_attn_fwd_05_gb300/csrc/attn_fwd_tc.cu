@@ -42,8 +42,12 @@
 //               longer read) -> TMA store, and LSE = (m + log2 l) ln 2.
 //
 // The launch is a list of items, one per (batch*head, 256-row query block),
-// batch*head fastest and heaviest causal blocks first, on a 1-D grid, so the
-// hardware's in-order dispatch acts as a longest-first schedule.  Items that
+// on a 1-D grid.  Heads go in groups whose K and V fit in half of L2, one group
+// after the other; inside a group batch*head is fastest and the heaviest
+// causal blocks come first, so the hardware's in-order dispatch acts as a
+// longest-first schedule and the CTAs running together re-read K and V from
+// L2 (at N = 16384, d = 128: 0.81 GB of DRAM traffic per launch instead of
+// 2.27 GB with all heads in one group, for 0.54 GB of inputs and outputs).  Items that
 // would leave a last wave at most half full (without the causal mask), or all
 // items of a grid that fills at most half the SMs, go to a second launch of
 // attn_fwd_bf16_tc_split_kernel: two CTAs per item, each on one 128-row half,
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const __grid_constant__ CUtensorMap tmV,
                             const __grid_constant__ CUtensorMap tmO, float *__restrict__ lse,
                             int N, int BH, int num_cta_tiles, float scale_log2, int causal,
-                            uint32_t *status, uint64_t timeout_ns, int num_sms) {
+                            uint32_t *status, uint64_t timeout_ns, int num_sms, int GH) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -305,9 +309,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // Items in launch order: batch*head fastest, heaviest causal tiles first.
-    const int bh = (int)blockIdx.x % BH;
-    const int cta_tile =
-        causal ? (num_cta_tiles - 1 - (int)blockIdx.x / BH) : (int)blockIdx.x / BH;
+    // Items in launch order: heads in groups of GH, one group after the other;
+    // inside a group batch*head fastest, heaviest causal tiles first.
+    auto decode = [&](int it, int &bh_, int &tile_) {
+        const int per_group = GH * num_cta_tiles;
+        const int g = it / per_group, rem = it - g * per_group;
+        const int gh = min(GH, BH - g * GH);
+        const int y = rem / gh;
+        bh_ = g * GH + (rem - y * gh);
+        tile_ = causal ? (num_cta_tiles - 1 - y) : y;
+    };
+    int bh, cta_tile;
+    decode((int)blockIdx.x, bh, cta_tile);
     const int row0 = cta_tile * (2 * BM);
     int TA, TB;
     tile_counts(N, cta_tile, causal, TA, TB);
@@ -352,8 +365,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the one num_sms further on).
         const int next = (int)blockIdx.x + num_sms;
         if (next < (int)gridDim.x) {
-            const int nbh = next % BH, ny = next / BH;
-            const int ntile = causal ? (num_cta_tiles - 1 - ny) : ny;
+            int nbh, ntile;
+            decode(next, nbh, ntile);
             for (int x = 0; x < 2; ++x) {
                 const int r = ntile * (2 * BM) + x * BM;
                 if (r < N)
@@ -914,11 +927,20 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
         if (rem > 0 && 2 * rem <= sms) n_split = rem;
     }
     const int64_t n_main = n_items - n_split;
+    // Heads per group: the K and V of one group fit in half of L2, so the
+    // CTAs that run together re-read K and V from L2 rather than HBM.  With
+    // split CTAs (which take the last items in batch*head-fastest order) the
+    // order stays ungrouped.
+    const int64_t kv_head = 4 * N * (int64_t)D;
+    int64_t gh64 = (64ll << 20) / (kv_head > 0 ? kv_head : 1);
+    if (gh64 < 1) gh64 = 1;
+    if (gh64 > BH || n_split > 0) gh64 = BH;
+    const int gh = (int)gh64;
     const float scale_log2 = scale * 1.44269504088896340736f;
     if (n_main > 0) {
         attn_fwd_bf16_tc_kernel<D><<<(unsigned)n_main, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
             tq, tk, tv, to, lse, (int)N, (int)BH, num_cta_tiles, scale_log2, causal ? 1 : 0,
-            ctx.status, ctx.timeout_ns, ctx.sm_count);
+            ctx.status, ctx.timeout_ns, ctx.sm_count, gh);
         const attn_status st = check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
         if (st != ATTN_OK) return st;
     }
