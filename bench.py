@@ -52,6 +52,25 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over all ranks of the initialised
+    process group (the slowest rank's time is the job's time); the values
+    themselves with one rank."""
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64)
+    import torch.distributed as tdist
+    if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
+        if device is not None:
+            t = t.to(device)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Throughput of the whole job: every rank processes `units_per_rank`
+    (weak scaling) and the job takes the slowest rank's `seconds`."""
+    return units_per_rank * world / seconds
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -357,16 +376,11 @@ def run_ours(args, w):
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = od.numel() * od.element_size() + lse.numel() * 4
 
-    local_ms = torch.tensor([step_ms, e2e_s * 1e3], dtype=torch.float64)
-    if world > 1:
-        t = local_ms.to(dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        local_ms = t.cpu()
-    step_ms, e2e_ms = float(local_ms[0]), float(local_ms[1])
+    step_ms, e2e_ms = max_over_ranks([step_ms, e2e_s * 1e3], device=dev)
     if rank != 0:
         return
-    tflops = w.flops * world / (step_ms * 1e-3) / 1e12
-    e2e_tflops = w.flops * world / (e2e_ms * 1e-3) / 1e12
+    tflops = whole_job_rate(w.flops, world, step_ms * 1e-3) / 1e12
+    e2e_tflops = whole_job_rate(w.flops, world, e2e_ms * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
     sustained = region_ms > 1000.0

@@ -152,6 +152,31 @@ def test_parity_workload(name):
     assert_close(w.dtype, of, lf, o_ref, lse_ref, vmax, name)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_parity_head_groups_with_partial_last_group(causal):
+    """B=1 H=11 N=16384 d=128: K and V of all heads exceed 64 MB, so heads are
+    dispatched in groups of 8 and 3 (every item of the partial group, every
+    head and the tile edges checked on sampled rows, plus whole tiles at the
+    start and end of the last head)."""
+    B, H, N, d = 1, 11, 16384, 128
+    q, k, v = make_qkv(B, H, N, d, seed=77, dtype="bf16")
+    scale = _scale(d)
+    o, lse = run_gpu(q, k, v, scale, causal)
+    rng = np.random.default_rng(77)
+    rows = sorted({0, 1, 127, 128, 255, 256, 257, 8191, 8192, N - 129, N - 128, N - 1}
+                  | set(rng.integers(0, N, size=12).tolist()))
+    bh_idx = np.repeat(np.arange(B * H), len(rows))
+    row_idx = np.tile(np.array(rows), B * H)
+    edge = np.concatenate([np.arange(0, 128), np.arange(N - 128, N)])
+    bh_idx = np.concatenate([bh_idx, np.full(edge.shape, B * H - 1)])
+    row_idx = np.concatenate([row_idx, edge])
+    o_ref, lse_ref = oracle.attn_fwd_rows(q, k, v, scale, causal, bh_idx, row_idx)
+    of = o.reshape(B * H, N, d)[bh_idx, row_idx]
+    lf = lse.reshape(B * H, N)[bh_idx, row_idx]
+    assert_close("bf16", of, lf, o_ref, lse_ref, float(v.float().abs().max()),
+                 f"H=11 N=16384 causal={causal}")
+
+
 # --------------------------------------------------- GPU invariances ---
 
 def test_t3g_key_shift_on_gpu():
