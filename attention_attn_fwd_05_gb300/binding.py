@@ -24,7 +24,8 @@ STATUS_NAMES = {
     4: "ATTN_ERR_HEADDIM", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_ARCH", 7: "ATTN_ERR_LAUNCH",
     8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
 }
-EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_row_softmax", "attn_add_rmsnorm", "attn_device_status",
+EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
+            "attn_bwd", "attn_row_softmax", "attn_add_rmsnorm", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_last_cuda_error", "attn_status_string",
             "attn_version")
 
@@ -58,6 +59,10 @@ def lib():
         L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                ctypes.c_int, ctypes.c_int, vp]
         L.attn_fwd_noalloc.argtypes = list(L.attn_fwd.argtypes)
+        L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                                    ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+        L.attn_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.c_int]
+        L.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
         L.attn_row_softmax.argtypes = [vp, vp, vp, i64, i64, vp]
         L.attn_bwd.argtypes = [vp] * 10 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
                                           ctypes.c_int, vp]
@@ -70,7 +75,8 @@ def lib():
         L.attn_status_string.argtypes = [ctypes.c_int]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_version.argtypes = []
-        for name in ("attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_row_softmax",
+        for name in ("attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_bwd",
+                     "attn_row_softmax",
                      "attn_add_rmsnorm",
                      "attn_device_status",
                      "attn_selftest_wait_timeout", "attn_version"):
@@ -152,50 +158,48 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                   stream: Optional[torch.cuda.Stream] = None,
                   buffers: Optional[dict] = None
                   ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """End-to-end call from host memory: copy Q, K, V to the device, run
-    attn_fwd, copy O and LSE back, all on one stream.
+    """End-to-end call from host memory through the C ABI's attn_fwd_host: Q,
+    K, V are copied to the device, the forward runs and O, LSE are copied back,
+    pipelined over chunks of batch*head so the copies overlap the kernels.
 
-    q, k, v: CPU tensors [B, H, N, d] (pinned memory gives asynchronous copies).
-    ``buffers`` may carry reusable device and pinned-host tensors (keys q, k, v,
-    o, lse, o_host, lse_host) so repeated calls do not allocate.  Returns CPU
-    (O, LSE); the call returns after the result is on the host.
+    q, k, v: contiguous CPU tensors [B, H, N, d] (pinned memory lets the copies
+    overlap).  ``buffers`` may carry the reusable device workspace and pinned
+    host outputs (keys ws, o_host, lse_host) so repeated calls do not allocate.
+    Returns CPU (O, LSE); the call returns after the result is on the host.
     """
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or t.is_cuda:
-            raise ValueError(f"{name} must be a CPU tensor")
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [B, H, N, d] tensors of one shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    code = _dtype_code(q.dtype)
     device = torch.device(device if device is not None else "cuda")
     bufs = buffers if buffers is not None else {}
     B, H, N, d = q.shape
-
-    def _buf(key, like, dev, pin=False, shape=None, dtype=None):
-        t = bufs.get(key)
-        shp = tuple(shape if shape is not None else like.shape)
-        dt = dtype if dtype is not None else like.dtype
-        if t is None or tuple(t.shape) != shp or t.dtype != dt:
-            if dev.type == "cuda":
-                t = torch.empty(shp, dtype=dt, device=dev)
-            else:
-                t = torch.empty(shp, dtype=dt, pin_memory=pin)
-            bufs[key] = t
-        return t
-
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     with torch.cuda.device(device):
+        nbytes = int(lib().attn_fwd_host_workspace_bytes(B, H, N, d, code))
+        if nbytes == 0:
+            _check(2, "attn_fwd_host_workspace_bytes")  # ATTN_ERR_SHAPE
+        ws = bufs.get("ws")
+        if ws is None or ws.device != device or ws.numel() < nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            bufs["ws"] = ws
+        oh = bufs.get("o_host")
+        if oh is None or tuple(oh.shape) != tuple(q.shape) or oh.dtype != q.dtype:
+            oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+            bufs["o_host"] = oh
+        lh = bufs.get("lse_host")
+        if lh is None or tuple(lh.shape) != (B, H, N):
+            lh = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+            bufs["lse_host"] = lh
         s = stream if stream is not None else torch.cuda.current_stream(device)
-        with torch.cuda.stream(s):
-            qd = _buf("q", q, device)
-            kd = _buf("k", k, device)
-            vd = _buf("v", v, device)
-            qd.copy_(q, non_blocking=True)
-            kd.copy_(k, non_blocking=True)
-            vd.copy_(v, non_blocking=True)
-            od = _buf("o", q, device)
-            ld = _buf("lse", q, device, shape=(B, H, N), dtype=torch.float32)
-            attn_fwd(qd, kd, vd, scale, causal, out=od, lse=ld, stream=s)
-            oh = _buf("o_host", q, torch.device("cpu"), pin=True)
-            lh = _buf("lse_host", q, torch.device("cpu"), pin=True, shape=(B, H, N),
-                      dtype=torch.float32)
-            oh.copy_(od, non_blocking=True)
-            lh.copy_(ld, non_blocking=True)
+        st = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), oh.data_ptr(),
+                                 lh.data_ptr(), B, H, N, d, scale, 1 if causal else 0, code,
+                                 ws.data_ptr(), nbytes, _stream_handle(s, device))
+        _check(st, "attn_fwd_host")
         s.synchronize()
     return oh, lh
 

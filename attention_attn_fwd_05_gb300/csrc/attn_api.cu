@@ -18,12 +18,20 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per barrier wait
 
+constexpr int kHostMaxChunks = 8;  // attn_fwd_host: chunks of batch*head per call
+
 struct DeviceState {
     bool ready = false;
     attn_status init_status = ATTN_OK;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     uint32_t *status = nullptr;  // 256 bytes of device memory, first word used
+    // attn_fwd_host: copy streams and events, made on its first call; `host_mu`
+    // serialises the calls that enqueue work on them.
+    bool host_ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev[2 + 2 * kHostMaxChunks] = {};
+    std::mutex host_mu;
 };
 
 std::mutex g_mu;
@@ -127,6 +135,140 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     return launch_attn_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                                static_cast<const float *>(v), static_cast<float *>(o), lse, BH, N,
                                (int)d, scale, causal != 0, ctx);
+}
+
+namespace {
+
+// Validation shared by attn_fwd and attn_fwd_host (no pointer checks).
+attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtype) {
+    if (B < 1 || H < 1 || N < 1 || N > INT32_MAX || !product_fits(B, H, N, d > 0 ? d : 1))
+        return ATTN_ERR_SHAPE;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
+    if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+    const int64_t BH = B * H;
+    if (dtype == ATTN_BF16 &&
+        (N > kMaxNBf16 || BH > INT32_MAX || BH * ((N + 255) / 256) > INT32_MAX))
+        return ATTN_ERR_SHAPE;
+    if (dtype == ATTN_F32 && (BH > 65535 || (N + 31) / 32 > INT32_MAX)) return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace layout of attn_fwd_host: Q, K, V, O, LSE, each 256-byte aligned.
+struct HostLayout {
+    size_t tensor, lse, total;
+};
+HostLayout host_layout(int64_t B, int64_t H, int64_t N, int64_t d, int dtype) {
+    const size_t elt = dtype == ATTN_F32 ? 4 : 2;
+    const size_t tensor = round256((size_t)(B * H * N * d) * elt);
+    const size_t lse = round256((size_t)(B * H * N) * 4);
+    return {tensor, lse, 4 * tensor + lse};
+}
+
+attn_status host_setup(DeviceState &s) {
+    if (s.host_ready) return ATTN_OK;
+    if (cudaStreamCreateWithFlags(&s.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&s.s_out, cudaStreamNonBlocking) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    for (cudaEvent_t &e : s.ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    s.host_ready = true;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" size_t attn_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d,
+                                                int dtype) {
+    if (check_fwd_shape(B, H, N, d, dtype) != ATTN_OK) return 0;
+    return host_layout(B, H, N, d, dtype).total;
+}
+
+extern "C" attn_status attn_fwd_host(const void *q, const void *k, const void *v, void *o,
+                                     float *lse, int64_t B, int64_t H, int64_t N, int64_t d,
+                                     float scale, int causal, int dtype, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !workspace) return ATTN_ERR_NULL;
+    attn_status st = check_fwd_shape(B, H, N, d, dtype);
+    if (st != ATTN_OK) return st;
+    const HostLayout lay = host_layout(B, H, N, d, dtype);
+    if (workspace_bytes < lay.total) return ATTN_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
+    DeviceState *s = nullptr;
+    if ((st = device_state(&s)) != ATTN_OK) return st;
+    if ((st = check_device_ptr(workspace)) != ATTN_OK) return st;
+    std::lock_guard<std::mutex> lk(s->host_mu);
+    if ((st = host_setup(*s)) != ATTN_OK) return st;
+
+    const int64_t BH = B * H;
+    const size_t elt = dtype == ATTN_F32 ? 4 : 2;
+    const size_t head = (size_t)N * (size_t)d * elt, head_lse = (size_t)N * 4;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *dq = ws, *dk = ws + lay.tensor, *dv = ws + 2 * lay.tensor, *dout = ws + 3 * lay.tensor;
+    float *dlse = reinterpret_cast<float *>(ws + 4 * lay.tensor);
+    // Chunks of consecutive (batch, head) pairs, about 16 MB of copies or more
+    // each, at most kHostMaxChunks: the copy in of chunk c+1, the forward of
+    // chunk c and the copy out of chunk c-1 overlap.
+    const size_t bytes = (size_t)BH * (4 * head + head_lse);
+    int64_t nc = (int64_t)(bytes / (16u << 20));
+    if (nc > kHostMaxChunks) nc = kHostMaxChunks;
+    if (nc > BH) nc = BH;
+    if (nc < 1) nc = 1;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaEvent_t e_start = s->ev[0], e_done = s->ev[1];
+    const LaunchCtx ctx = make_ctx(*s, stream, kDefaultTimeoutNs);
+    // Work already on `stream` (earlier users of the workspace or the host
+    // buffers) comes first.
+    if ((st = check_launch(cudaEventRecord(e_start, cs), ATTN_ERR_CUDA)) != ATTN_OK ||
+        (st = check_launch(cudaStreamWaitEvent(s->s_in, e_start, 0), ATTN_ERR_CUDA)) !=
+            ATTN_OK ||
+        (st = check_launch(cudaStreamWaitEvent(s->s_out, e_start, 0), ATTN_ERR_CUDA)) != ATTN_OK)
+        return st;
+    for (int64_t c = 0; c < nc; ++c) {
+        const int64_t h0 = BH * c / nc, h1 = BH * (c + 1) / nc, nh = h1 - h0;
+        const size_t off = (size_t)h0 * head, len = (size_t)nh * head;
+        cudaEvent_t e_in = s->ev[2 + 2 * c], e_comp = s->ev[3 + 2 * c];
+        // One copy per tensor and chunk.
+        for (int t = 0; t < 3; ++t) {
+            const uint8_t *src = static_cast<const uint8_t *>(t == 0 ? q : (t == 1 ? k : v));
+            uint8_t *dst = t == 0 ? dq : (t == 1 ? dk : dv);
+            if ((st = check_launch(cudaMemcpyAsync(dst + off, src + off, len, cudaMemcpyDefault,
+                                                   s->s_in),
+                                   ATTN_ERR_CUDA)) != ATTN_OK)
+                return st;
+        }
+        if ((st = check_launch(cudaEventRecord(e_in, s->s_in), ATTN_ERR_CUDA)) != ATTN_OK ||
+            (st = check_launch(cudaStreamWaitEvent(cs, e_in, 0), ATTN_ERR_CUDA)) != ATTN_OK)
+            return st;
+        float *lse_c = lse ? dlse + h0 * N : nullptr;
+        st = dtype == ATTN_BF16
+                 ? launch_attn_fwd_bf16(dq + off, dk + off, dv + off, dout + off, lse_c, nh, N,
+                                        (int)d, scale, causal != 0, ctx)
+                 : launch_attn_fwd_f32(reinterpret_cast<const float *>(dq + off),
+                                       reinterpret_cast<const float *>(dk + off),
+                                       reinterpret_cast<const float *>(dv + off),
+                                       reinterpret_cast<float *>(dout + off), lse_c, nh, N,
+                                       (int)d, scale, causal != 0, ctx);
+        if (st != ATTN_OK) return st;
+        if ((st = check_launch(cudaEventRecord(e_comp, cs), ATTN_ERR_CUDA)) != ATTN_OK ||
+            (st = check_launch(cudaStreamWaitEvent(s->s_out, e_comp, 0), ATTN_ERR_CUDA)) !=
+                ATTN_OK ||
+            (st = check_launch(cudaMemcpyAsync(static_cast<uint8_t *>(o) + off, dout + off, len,
+                                               cudaMemcpyDefault, s->s_out),
+                               ATTN_ERR_CUDA)) != ATTN_OK)
+            return st;
+        if (lse &&
+            (st = check_launch(cudaMemcpyAsync(lse + h0 * N, lse_c, (size_t)nh * head_lse,
+                                               cudaMemcpyDefault, s->s_out),
+                               ATTN_ERR_CUDA)) != ATTN_OK)
+            return st;
+    }
+    // Everything, the last copy out included, is ordered before later work on `stream`.
+    if ((st = check_launch(cudaEventRecord(e_done, s->s_out), ATTN_ERR_CUDA)) != ATTN_OK)
+        return st;
+    return check_launch(cudaStreamWaitEvent(cs, e_done, 0), ATTN_ERR_CUDA);
 }
 
 extern "C" attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,
@@ -238,4 +380,4 @@ extern "C" const char *attn_last_cuda_error(void) {
     return cudaGetErrorString(t_last_error);
 }
 
-extern "C" int attn_version(void) { return 10000; }
+extern "C" int attn_version(void) { return 10100; }

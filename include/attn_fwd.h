@@ -31,6 +31,7 @@
 #ifndef ATTN_FWD_GB300_H
 #define ATTN_FWD_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -112,6 +113,50 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
 attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                              int64_t B, int64_t H, int64_t N, int64_t d, float scale,
                              int causal, int dtype, void *stream);
+
+/*
+ * attn_fwd_host_workspace_bytes -- bytes of device workspace attn_fwd_host
+ * needs for this problem: room for Q, K, V and O in `dtype` and LSE in fp32,
+ * each rounded up to 256 bytes.  0 when the arguments are invalid for
+ * attn_fwd.
+ */
+size_t attn_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int dtype);
+
+/*
+ * attn_fwd_host -- attn_fwd from and to host memory.  Q, K and V are copied to
+ * the device, the forward runs, and O and LSE are copied back.  The problem
+ * is cut into chunks of consecutive (batch, head) pairs (up to 8, each about
+ * 16 MB of copies or more).  Copying chunk c+1 in, computing chunk c and
+ * copying chunk c-1 out run at the same time: the library keeps two copy
+ * streams per device beside `stream`, ordered with events, and issues one
+ * cudaMemcpyAsync per tensor and chunk.
+ *
+ *   q, k, v    [B,H,N,d] inputs in `dtype`, read only.  Host memory: page-locked
+ *              (pinned) memory lets the copies overlap; pageable memory works,
+ *              but its copies do not overlap.  Any pointer the CUDA runtime can
+ *              copy from with cudaMemcpyDefault is accepted.
+ *   o          [B,H,N,d] output in `dtype`, host memory as above, fully
+ *              overwritten.
+ *   lse        [B,H,N] fp32 output in host memory, or NULL to skip it.
+ *   workspace  device memory of the current device, 256-byte aligned, at least
+ *              attn_fwd_host_workspace_bytes(B,H,N,d,dtype) bytes.  The caller
+ *              owns it; the call holds no reference once the work is done.
+ *   workspace_bytes  its size.
+ *   B, H, N, d, scale, causal, dtype, stream   as attn_fwd.
+ *
+ * Asynchronous like attn_fwd.  The work is ordered after what `stream` already
+ * holds, and everything the call enqueues, the last copy out included, is
+ * ordered before later work on `stream`.  The outputs are on the host once
+ * `stream` has been synchronised.  The first call on a device creates the two
+ * copy streams and 18 events.  Calls from several host threads are
+ * serialised while they enqueue.  No device memory is allocated.
+ * Returns ATTN_OK or the first validation / launch error: ATTN_ERR_NULL for a
+ * NULL q, k, v, o or workspace; ATTN_ERR_SHAPE also for a workspace that is
+ * too small; ATTN_ERR_ALIGN for a workspace that is not 256-byte aligned.
+ */
+attn_status attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                          int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * attn_row_softmax -- row softmax of a [rows, width] fp32 matrix in one pass

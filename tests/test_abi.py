@@ -39,7 +39,7 @@ def test_status_strings_and_version(L):
     for code in range(11):
         assert L.attn_status_string(code)
     assert L.attn_status_string(999) == b"unknown status"
-    assert L.attn_version() == 10000
+    assert L.attn_version() == 10100
 
 
 # Fake, never-dereferenced addresses: validation must reject these calls
@@ -133,3 +133,26 @@ def test_attn_bwd_validation(L):
     bad = list(args)
     bad[6] = A + 4
     assert L.attn_bwd(*bad, 1, 1, 8, 64, f, 0, 1, None) == 5
+
+
+def test_fwd_host_rejects_bad_arguments_on_the_host(L):
+    """attn_fwd_host validates before touching CUDA: NULL pointers, shapes,
+    a workspace that is too small or misaligned."""
+    ws_need = L.attn_fwd_host_workspace_bytes(1, 2, 300, 64, 1)
+    # Q, K, V, O at 2 B per element and LSE at 4 B, each rounded up to 256 B.
+    assert ws_need == 4 * 76800 + 2560
+    assert L.attn_fwd_host_workspace_bytes(1, 2, 300, 65, 1) == 0
+    assert L.attn_fwd_host_workspace_bytes(0, 2, 300, 64, 1) == 0
+    assert L.attn_fwd_host_workspace_bytes(1, 2, 300, 64, 7) == 0
+
+    def host(q=A, k=A, v=A, o=A + 0x100000, ws=A + 0x200000, nbytes=ws_need, N=300, d=64,
+             dtype=1):
+        return L.attn_fwd_host(q, k, v, o, None, 1, 2, N, d, ctypes.c_float(0.125), 1, dtype,
+                               ws, nbytes, None)
+    assert host(q=None) == 1
+    assert host(o=None) == 1
+    assert host(ws=None) == 1
+    assert host(d=96) == 4
+    assert host(dtype=5) == 3
+    assert host(nbytes=ws_need - 1) == 2
+    assert host(ws=A + 0x200080) == 5

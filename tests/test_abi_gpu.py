@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from attention_attn_fwd_05_gb300 import (attn_fwd, binding, device_status, row_softmax,
+from attention_attn_fwd_05_gb300 import (attn_fwd, attn_fwd_host, binding, device_status, row_softmax,
                                          selftest_wait_timeout)
 from attention_attn_fwd_05_gb300.inputs import make_qkv, make_rows
 
@@ -109,3 +109,64 @@ def test_row_softmax_masked_and_in_place():
     yd = xd.cpu().numpy().astype(np.float64)
     assert (yd[:, ::7] == 0).all()
     assert np.all(np.abs(yd - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)
+
+
+# ------------------------------------------------ attn_fwd_host (host memory) ---
+
+@pytest.mark.parametrize("dtype,B,H,N,d,causal", [
+    ("bf16", 1, 2, 300, 64, True),       # one chunk
+    ("bf16", 2, 16, 2048, 128, False),   # eight chunks
+    ("bf16", 1, 11, 4096, 128, True),    # two uneven chunks (5 and 6 heads)
+    ("f32", 1, 8, 1024, 64, False),      # one chunk, exact fp32 kernel
+    ("f32", 2, 8, 2048, 64, True),       # four chunks, exact fp32 kernel
+])
+def test_fwd_host_matches_device_call(dtype, B, H, N, d, causal):
+    """The pipelined host-memory call against the device call on the same
+    values.  A problem copied in one chunk runs the very same launch: equal
+    bit for bit.  Chunks are launched on fewer heads, which can change the
+    launch shape (split CTAs for small chunks) and with it the fp32 summation
+    order: then both are held to the parity tolerances."""
+    q, k, v = make_qkv(B, H, N, d, seed=B * 100 + H + N, dtype=dtype)
+    scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    o_dev, lse_dev = attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale, causal)
+    torch.cuda.synchronize()
+    o_dev, lse_dev = o_dev.cpu(), lse_dev.cpu()
+    elt = 2 if dtype == "bf16" else 4
+    one_chunk = B * H * (4 * N * d * elt + 4 * N) < (32 << 20)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    bufs = {}
+    for _ in range(2):  # the second call reuses the workspace and host outputs
+        o_h, lse_h = attn_fwd_host(qh, kh, vh, scale, causal, buffers=bufs)
+        assert device_status() == 0
+        if one_chunk:
+            assert torch.equal(o_h, o_dev) and torch.equal(lse_h, lse_dev)
+            continue
+        do = (o_h.float() - o_dev.float()).abs()
+        dl = (lse_h - lse_dev).abs().max().item()
+        if dtype == "bf16":
+            assert do.max().item() <= 2e-2 and dl <= 1e-3
+        else:
+            tol = 1e-5 * v.abs().max().item() + 1e-5 * o_dev.abs()
+            assert bool((do <= tol).all()) and dl <= 2e-5 + 1e-5 * lse_dev.abs().max().item()
+
+
+def test_fwd_host_pageable_inputs_and_no_lse():
+    """Pageable host inputs work, and a NULL lse skips the LSE copy; O still
+    matches the device call."""
+    import ctypes
+    from attention_attn_fwd_05_gb300.binding import lib
+    B, H, N, d = 1, 4, 1000, 128
+    q, k, v = make_qkv(B, H, N, d, seed=5, dtype="bf16")
+    scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    o_dev, _ = attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale, False)
+    nbytes = lib().attn_fwd_host_workspace_bytes(B, H, N, d, 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    o_h = torch.empty_like(q)  # pageable
+    s = torch.cuda.current_stream()
+    st = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_h.data_ptr(), None,
+                             B, H, N, d, ctypes.c_float(scale), 0, 1, ws.data_ptr(), nbytes,
+                             s.cuda_stream)
+    assert st == 0
+    s.synchronize()
+    assert device_status() == 0
+    assert torch.equal(o_h, o_dev.cpu())
