@@ -61,14 +61,33 @@ __global__ void __launch_bounds__(NUM_THREADS)
         MD md{-INFINITY, 0.f};
         if (vec4) {
             const int64_t n4 = width / 4;
-            for (int64_t i = threadIdx.x; i < n4; i += NUM_THREADS) {
-                const float4 v = reinterpret_cast<const float4 *>(xr)[i];
-                if (cached) reinterpret_cast<float4 *>(cache)[i] = v;
-                const float gm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+            // Four float4 groups per step, loaded before any is used, so each
+            // thread keeps four loads in flight; the running pair is rescaled
+            // once per step.
+            constexpr int U = 4;
+            for (int64_t i0 = threadIdx.x; i0 < n4; i0 += U * NUM_THREADS) {
+                float4 v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = i0 + (int64_t)u * NUM_THREADS;
+                    v[u] = i < n4 ? reinterpret_cast<const float4 *>(xr)[i]
+                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+                float gm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = i0 + (int64_t)u * NUM_THREADS;
+                    if (cached && i < n4) reinterpret_cast<float4 *>(cache)[i] = v[u];
+                    gm = fmaxf(gm, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+                }
                 const float M = fmaxf(md.m, gm);
                 if (M == -INFINITY) continue;  // only masked (-inf) entries so far
-                md.d = md.d * expf(md.m - M) + expf(v.x - M) + expf(v.y - M) + expf(v.z - M) +
-                       expf(v.w - M);
+                float add = 0.f;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    add += (expf(v[u].x - M) + expf(v[u].y - M)) +
+                           (expf(v[u].z - M) + expf(v[u].w - M));
+                md.d = md.d * expf(md.m - M) + add;
                 md.m = M;
             }
         } else {
@@ -107,15 +126,24 @@ __global__ void __launch_bounds__(NUM_THREADS)
         const float M = dead ? 0.f : row_md.m, inv_d = dead ? 0.f : 1.f / row_md.d;
         if (vec4) {
             const int64_t n4 = width / 4;
-            for (int64_t i = threadIdx.x; i < n4; i += NUM_THREADS) {
-                const float4 v = cached ? reinterpret_cast<const float4 *>(cache)[i]
-                                        : reinterpret_cast<const float4 *>(xr)[i];
-                float4 o;
-                o.x = expf(v.x - M) * inv_d;
-                o.y = expf(v.y - M) * inv_d;
-                o.z = expf(v.z - M) * inv_d;
-                o.w = expf(v.w - M) * inv_d;
-                reinterpret_cast<float4 *>(yr)[i] = o;
+            constexpr int U = 4;
+            for (int64_t i0 = threadIdx.x; i0 < n4; i0 += U * NUM_THREADS) {
+                float4 v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = i0 + (int64_t)u * NUM_THREADS;
+                    if (i < n4)
+                        v[u] = cached ? reinterpret_cast<const float4 *>(cache)[i]
+                                      : reinterpret_cast<const float4 *>(xr)[i];
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = i0 + (int64_t)u * NUM_THREADS;
+                    if (i < n4)
+                        reinterpret_cast<float4 *>(yr)[i] =
+                            make_float4(expf(v[u].x - M) * inv_d, expf(v[u].y - M) * inv_d,
+                                        expf(v[u].z - M) * inv_d, expf(v[u].w - M) * inv_d);
+                }
             }
         } else {
             for (int64_t i = threadIdx.x; i < width; i += NUM_THREADS) {

@@ -67,7 +67,7 @@ def test_row_softmax_parity(rows, width):
     np.testing.assert_allclose(yd.sum(axis=1), 1.0, rtol=0, atol=1e-4)
 
 
-@pytest.mark.parametrize("rows,width", [(5, 513), (5000, 512)])
+@pytest.mark.parametrize("rows,width", [(5, 513), (5000, 512), (40, 20000)])
 def test_row_softmax_masked_and_in_place_both_paths(rows, width):
     """-inf entries get probability 0, in place, on either kernel."""
     x = make_rows(rows, width, seed=rows + 3, spread=3.0)
@@ -81,7 +81,7 @@ def test_row_softmax_masked_and_in_place_both_paths(rows, width):
     assert np.all(np.abs(yd - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)
 
 
-@pytest.mark.parametrize("width", [513, 512])
+@pytest.mark.parametrize("width", [513, 512, 20000])
 def test_row_softmax_fully_masked_row(width):
     """A row of -inf only: every probability 0 and LSE = -inf; other rows unaffected."""
     n = 3000
