@@ -51,7 +51,9 @@
 // would leave a last wave at most half full (without the causal mask), or all
 // items of a grid that fills at most half the SMs, go to a second launch of
 // attn_fwd_bf16_tc_split_kernel: two CTAs per item, each on one 128-row half,
-// with tile A on the even and tile B on the odd key tiles (see there).
+// with tile A on the even and tile B on the odd key tiles (see there).  That
+// launch is a programmatic dependent of the first, so its CTAs start on the
+// SMs the main kernel's last wave leaves free.
 //
 // The N x N logits live only in TMEM and registers; device memory sees Q, K,
 // V read and O, LSE written.
@@ -321,6 +323,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     int bh, cta_tile;
     decode((int)blockIdx.x, bh, cta_tile);
+    // The split-CTA launch that may follow reads nothing this kernel writes:
+    // let it start on SMs this launch has finished with.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row0 = cta_tile * (2 * BM);
     int TA, TB;
     tile_counts(N, cta_tile, causal, TA, TB);
@@ -834,6 +839,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+    // This launch may start before the main kernel of the same call has
+    // finished; it completes only after it, so later work on the stream sees
+    // every output row.  (Returns at once without a preceding main kernel.)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // A kernel whose only job is to wait, through bounded_wait, on a barrier that
@@ -945,12 +954,21 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
         if (st != ATTN_OK) return st;
     }
     if (n_split > 0) {
-        attn_fwd_bf16_tc_split_kernel<D><<<(unsigned)(2 * n_split), NUM_THREADS, C::SMEM_BYTES,
-                                           ctx.stream>>>(tq, tk, tv, to, lse, (int)N, (int)BH,
-                                                         num_cta_tiles, (int)n_main, scale_log2,
-                                                         causal ? 1 : 0, ctx.status,
-                                                         ctx.timeout_ns);
-        return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * n_split));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = ctx.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = n_main > 0 ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return check_launch(cudaLaunchKernelEx(&cfg, attn_fwd_bf16_tc_split_kernel<D>, tq, tk, tv,
+                                               to, lse, (int)N, (int)BH, num_cta_tiles,
+                                               (int)n_main, scale_log2, causal ? 1 : 0,
+                                               ctx.status, ctx.timeout_ns),
+                            ATTN_ERR_LAUNCH);
     }
     return ATTN_OK;
 }
