@@ -45,6 +45,22 @@ def test_graph_with_several_launches():
         assert torch.equal(o, o_e) and torch.equal(lse, lse_e)
 
 
+def test_graph_with_main_and_split_launches():
+    """B=4 H=16 N=2048 d=128: 456 items in the main kernel and the last 56 in the
+    split-CTA kernel, launched as its programmatic dependent; captured and
+    replayed twice (the second replay right after the first, with nothing in
+    between), it gives exactly the eager call's outputs."""
+    q, k, v = (t.cuda() for t in make_qkv(4, 16, 2048, 128, seed=61, dtype="bf16"))
+    g = AttnGraph([(q, k, v, False)])
+    g.replay()
+    (o, lse), = g.replay()
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    o_e, lse_e = attn_fwd(q, k, v, causal=False)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_e) and torch.equal(lse, lse_e)
+
+
 def test_graph_replay_is_cheaper_on_the_host():
     """Host dispatch cost per call (time to enqueue, not to finish): a replay
     skips the eager call's argument checks, pointer queries and tensor-map
