@@ -27,6 +27,10 @@
 //         S = Q K^T,  dP = dO V^T;  dS = P (dP - D);  dQ += dS K,
 //       with S of the next block issued as soon as the row warps have read S.
 //
+// The dQ kernel is launched as a programmatic dependent of the dK/dV kernel:
+// it reads nothing the first one writes, so its CTAs start on SMs the first
+// one's last wave leaves free, and it completes only after it.
+//
 // S and dP are recomputed in the second kernel (7 GEMMs where a single pass
 // with atomic dQ updates would do 5) so that every output row has exactly one
 // writer.  P and dS are rounded to bf16 for the MMAs; every sum accumulates
@@ -207,6 +211,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int nq = (N + BN - 1) / BN;
     const int q0 = causal ? kb : 0;  // query blocks q0 .. nq-1 see this key block
     const int T = nq - q0;
+    // The dQ launch that follows reads nothing this kernel writes: let it
+    // start on SMs this launch has finished with.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_RES), 1);
@@ -594,6 +601,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+    // This launch may start before the dK/dV kernel of the same call has
+    // finished; it completes only after it.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D>
@@ -622,10 +632,22 @@ static attn_status launch(const void *q, const void *k, const void *v, const voi
         ctx.timeout_ns);
     attn_status st = check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
     if (st != ATTN_OK) return st;
-    bwd_dq_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
-        tq, tk, tv, tg, tdq, lse, delta, (int)N, scale, causal ? 1 : 0, ctx.status,
-        ctx.timeout_ns);
-    return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
+    // dQ as a programmatic dependent of dK/dV: both only read what earlier
+    // launches (D included) wrote, so dQ's CTAs may start early.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_launch(cudaLaunchKernelEx(&cfg, bwd_dq_tc_kernel<D>, tq, tk, tv, tg, tdq, lse,
+                                           delta, (int)N, scale, causal ? 1 : 0, ctx.status,
+                                           ctx.timeout_ns),
+                        ATTN_ERR_LAUNCH);
 }
 
 }  // namespace bwdtc
