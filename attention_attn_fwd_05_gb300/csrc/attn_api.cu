@@ -109,37 +109,10 @@ attn_status check_launch(cudaError_t e, attn_status on_error) {
 
 using namespace attn;
 
-extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-                                int64_t B, int64_t H, int64_t N, int64_t d, float scale,
-                                int causal, int dtype, void *stream) {
-    if (!q || !k || !v || !o) return ATTN_ERR_NULL;
-    if (B < 1 || H < 1 || N < 1 || N > INT32_MAX || !product_fits(B, H, N, d > 0 ? d : 1))
-        return ATTN_ERR_SHAPE;
-    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
-    if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
-    const int64_t BH = B * H;
-    if (dtype == ATTN_BF16 && (N > kMaxNBf16 || BH > INT32_MAX || BH * ((N + 255) / 256) > INT32_MAX))
-        return ATTN_ERR_SHAPE;
-    if (dtype == ATTN_F32 && (BH > 65535 || (N + 31) / 32 > INT32_MAX)) return ATTN_ERR_SHAPE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return ATTN_ERR_ALIGN;
-    DeviceState *s = nullptr;
-    attn_status st = device_state(&s);
-    if (st != ATTN_OK) return st;
-    for (const void *p : {q, k, v, static_cast<const void *>(o)})
-        if ((st = check_device_ptr(p)) != ATTN_OK) return st;
-    if (lse && (st = check_device_ptr(lse)) != ATTN_OK) return st;
-    const LaunchCtx ctx = make_ctx(*s, stream, kDefaultTimeoutNs);
-    if (dtype == ATTN_BF16)
-        return launch_attn_fwd_bf16(q, k, v, o, lse, BH, N, (int)d, scale, causal != 0, ctx);
-    return launch_attn_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
-                               static_cast<const float *>(v), static_cast<float *>(o), lse, BH, N,
-                               (int)d, scale, causal != 0, ctx);
-}
+namespace attn {
 
-namespace {
-
-// Validation shared by attn_fwd and attn_fwd_host (no pointer checks).
+// Shape, dtype and head-dim rules of attn_fwd, shared by every forward entry
+// point (no pointer checks).
 attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtype) {
     if (B < 1 || H < 1 || N < 1 || N > INT32_MAX || !product_fits(B, H, N, d > 0 ? d : 1))
         return ATTN_ERR_SHAPE;
@@ -152,6 +125,32 @@ attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtyp
     if (dtype == ATTN_F32 && (BH > 65535 || (N + 31) / 32 > INT32_MAX)) return ATTN_ERR_SHAPE;
     return ATTN_OK;
 }
+
+}  // namespace attn
+
+extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                                int causal, int dtype, void *stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_NULL;
+    attn_status st = check_fwd_shape(B, H, N, d, dtype);
+    if (st != ATTN_OK) return st;
+    const int64_t BH = B * H;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_ALIGN;
+    DeviceState *s = nullptr;
+    if ((st = device_state(&s)) != ATTN_OK) return st;
+    for (const void *p : {q, k, v, static_cast<const void *>(o)})
+        if ((st = check_device_ptr(p)) != ATTN_OK) return st;
+    if (lse && (st = check_device_ptr(lse)) != ATTN_OK) return st;
+    const LaunchCtx ctx = make_ctx(*s, stream, kDefaultTimeoutNs);
+    if (dtype == ATTN_BF16)
+        return launch_attn_fwd_bf16(q, k, v, o, lse, BH, N, (int)d, scale, causal != 0, ctx);
+    return launch_attn_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                               static_cast<const float *>(v), static_cast<float *>(o), lse, BH, N,
+                               (int)d, scale, causal != 0, ctx);
+}
+
+namespace {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 

@@ -66,4 +66,8 @@ attn_status check_launch(cudaError_t e, attn_status on_error);
 // Largest N the bf16 kernel's grid can cover (query tiles on grid.y).
 constexpr int64_t kMaxNBf16 = 65535LL * 128;
 
+// Shape, dtype and head-dim rules of attn_fwd (ATTN_OK or the error code),
+// shared by attn_fwd, attn_fwd_noalloc and attn_fwd_host.
+attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtype);
+
 }  // namespace attn

@@ -74,16 +74,6 @@ attn_status noalloc_setup(NoAllocDevice **out) {
 
 bool is_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool fits_2_62(int64_t a, int64_t b, int64_t c, int64_t d) {
-    const int64_t lim = (int64_t)1 << 62;
-    int64_t p = a;
-    for (int64_t f : {b, c, d}) {
-        if (p > lim / f) return false;
-        p *= f;
-    }
-    return p < lim;
-}
-
 attn_status device_pointer(const void *p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -107,20 +97,14 @@ extern "C" attn_status attn_fwd_noalloc(const void *q, const void *k, const void
                                         float scale, int causal, int dtype, void *stream) {
     // The same argument rules as attn_fwd.
     if (!q || !k || !v || !o) return ATTN_ERR_NULL;
-    if (B < 1 || H < 1 || N < 1 || N > INT32_MAX || !fits_2_62(B, H, N, d > 0 ? d : 1))
-        return ATTN_ERR_SHAPE;
-    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
-    if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+    attn_status st = check_fwd_shape(B, H, N, d, dtype);
+    if (st != ATTN_OK) return st;
     const int64_t BH = B * H;
-    if (dtype == ATTN_BF16 && (N > kMaxNBf16 || BH > INT32_MAX || BH * ((N + 255) / 256) > INT32_MAX))
-        return ATTN_ERR_SHAPE;
-    if (dtype == ATTN_F32 && (BH > 65535 || (N + 31) / 32 > INT32_MAX)) return ATTN_ERR_SHAPE;
     if (!is_aligned16(q) || !is_aligned16(k) || !is_aligned16(v) || !is_aligned16(o) ||
         !is_aligned16(lse))
         return ATTN_ERR_ALIGN;
     NoAllocDevice *s = nullptr;
-    attn_status st = noalloc_setup(&s);
-    if (st != ATTN_OK) return st;
+    if ((st = noalloc_setup(&s)) != ATTN_OK) return st;
     for (const void *p : {q, k, v, static_cast<const void *>(o)})
         if ((st = device_pointer(p)) != ATTN_OK) return st;
     if (lse && (st = device_pointer(lse)) != ATTN_OK) return st;
