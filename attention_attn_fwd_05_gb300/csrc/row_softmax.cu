@@ -19,6 +19,10 @@
 //   pass 1 takes its maximum m_t and e = exp(x - m_t), the CTA merges the
 //   (m_t, sum e) pairs into (M, D), and pass 2 writes y = e * exp(m_t - M) / D,
 //   one exponential per element in all.
+// row_softmax_cluster_kernel -- aligned rows longer than kStreamMaxWidth
+//   when there are too few of them to fill the GPU one CTA per row: a
+//   thread-block cluster of CTAs per row, merged through distributed shared
+//   memory (see there).
 // row_softmax_kernel -- any other row: pass 1 walks the row updating (m, d)
 //   per 4-element group; pass 2 writes the output, reading the row from shared
 //   memory when it was cached there in pass 1 (rows up to kCacheFloats),
@@ -313,6 +317,182 @@ attn_status launch_stream(const float *x, float *y, float *lse, int64_t rows, in
     return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 
+// ------------------------------------------------------------- clusters ---
+// Aligned rows longer than kStreamMaxWidth when there are too few of them for
+// one CTA per row to fill the GPU: a cluster of CL CTAs (2..8) per row, CTA
+// `rank` taking the slice [rank, rank + 1) * width / CL.  Each CTA reduces its
+// slice to one (m, d) pair, stores it into slot `rank` of every cluster CTA's
+// shared memory and arrives on their barriers; once a CTA's barrier has all CL
+// arrivals it merges the pairs (in rank order, the same in every CTA) and
+// writes y for its slice.  Rows alternate between two barriers and two sets of
+// slots, so a CTA one row ahead never overwrites slots still being read.  Every
+// wait is bounded, and a cluster barrier before exit keeps each CTA's shared
+// memory alive until no other CTA of the cluster can still store into it.
+
+constexpr int CL_THREADS = 512;
+constexpr int CL_MAX = 8;
+
+struct ClusterSmem {
+    uint64_t xbar[2];            // per row parity: CL arrivals, one per cluster CTA
+    MD pairs[2][CL_MAX];         // per row parity: (m, d) of every cluster CTA
+    MD warp_md[CL_THREADS / 32];
+    MD cta_md;
+    uint32_t abort;
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
+                 : "memory");
+}
+__device__ __forceinline__ void arrive_remote(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+// Bounded wait on a barrier that other CTAs of the cluster arrive on: gives up
+// after `timeout_ns`, or at once when a timeout is already recorded.
+__device__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, uint32_t *status,
+                                     uint64_t timeout_ns) {
+    if (try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (try_wait_cluster(bar, parity)) return true;
+        if ((n & 63u) == 0u) {
+            if (*reinterpret_cast<volatile uint32_t *>(status) & STATUS_TIMEOUT) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                atomicOr(status, STATUS_TIMEOUT);
+                __threadfence();
+                return false;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(CL_THREADS)
+    row_softmax_cluster_kernel(const float *x, float *y, float *__restrict__ lse, int64_t rows,
+                               int width, int CL, uint32_t *status, uint64_t timeout_ns) {
+    __shared__ ClusterSmem sm;
+    const uint32_t rank = cluster_ctarank();
+    const int64_t cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&sm.xbar[0]), (uint32_t)CL);
+        mbar_init(smem_u32(&sm.xbar[1]), (uint32_t)CL);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // Every CTA's barriers are initialised before any CTA arrives on them.
+    cluster_sync_all();
+    const int64_t n4 = width / 4;
+    const int64_t c0 = n4 * rank / CL, c1 = n4 * (rank + 1) / CL;
+    constexpr int U = 4;
+    int it = 0;
+    for (int64_t r = cid; r < rows; r += ncl, ++it) {
+        const int par = it & 1;
+        const float4 *xr = reinterpret_cast<const float4 *>(x + r * (int64_t)width);
+        // Pass 1 over this CTA's slice: a running (m, d), four groups per step.
+        MD md{-INFINITY, 0.f};
+        for (int64_t i0 = c0 + threadIdx.x; i0 < c1; i0 += U * CL_THREADS) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * CL_THREADS;
+                v[u] = i < c1 ? xr[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            float gm = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                gm = fmaxf(gm, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+            const float M = fmaxf(md.m, gm);
+            if (M == -INFINITY) continue;
+            float add = 0.f;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                add += (expf(v[u].x - M) + expf(v[u].y - M)) + (expf(v[u].z - M) + expf(v[u].w - M));
+            md.d = md.d * expf(md.m - M) + add;
+            md.m = M;
+        }
+        const MD wmd = merge_group(md.m, md.d);
+        if (lane == 0) sm.warp_md[warp] = wmd;
+        __syncthreads();
+        if (warp == 0) {
+            const MD w = lane < CL_THREADS / 32 ? sm.warp_md[lane] : MD{-INFINITY, 0.f};
+            const MD tot = merge_group(w.m, w.d);
+            if (lane == 0) {
+                // This CTA's pair into slot `rank` of every cluster CTA, then
+                // one arrival on each of their barriers for this row.
+                const uint32_t slot = smem_u32(&sm.pairs[par][rank]);
+                const uint32_t xb = smem_u32(&sm.xbar[par]);
+                for (int dst = 0; dst < CL; ++dst) {
+                    st_cluster_f32x2(map_shared_to_rank(slot, (uint32_t)dst), tot.m, tot.d);
+                    arrive_remote(map_shared_to_rank(xb, (uint32_t)dst));
+                }
+            }
+        }
+        bool ok = true;
+        if (lane == 0)
+            ok = wait_cluster_bounded(smem_u32(&sm.xbar[par]), (uint32_t)(it >> 1) & 1u, status,
+                                      timeout_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!__syncthreads_and(ok ? 1 : 0)) break;
+        // Every slice's pair, merged in rank order.
+        float M = -INFINITY;
+        for (int c = 0; c < CL; ++c) M = fmaxf(M, sm.pairs[par][c].m);
+        float D = 0.f;
+        if (M != -INFINITY)
+            for (int c = 0; c < CL; ++c)
+                if (sm.pairs[par][c].m != -INFINITY)
+                    D += sm.pairs[par][c].d * expf(sm.pairs[par][c].m - M);
+        if (rank == 0 && threadIdx.x == 0 && lse != nullptr) lse[r] = M + logf(D);
+        // A row of -inf only has M = -inf and D = 0: every probability is 0.
+        const bool dead = M == -INFINITY;
+        const float Ms = dead ? 0.f : M, inv_d = dead ? 0.f : 1.f / D;
+        float4 *yr = reinterpret_cast<float4 *>(y + r * (int64_t)width);
+        for (int64_t i0 = c0 + threadIdx.x; i0 < c1; i0 += U * CL_THREADS) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * CL_THREADS;
+                if (i < c1) v[u] = xr[i];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * CL_THREADS;
+                if (i < c1)
+                    yr[i] = make_float4(expf(v[u].x - Ms) * inv_d, expf(v[u].y - Ms) * inv_d,
+                                        expf(v[u].z - Ms) * inv_d, expf(v[u].w - Ms) * inv_d);
+            }
+        }
+        __syncthreads();  // warp_md is reused by the next row
+    }
+    // No CTA leaves while another CTA of the cluster may still store into its
+    // shared memory.
+    cluster_sync_all();
+}
+
 }  // namespace rsm
 
 attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t rows, int64_t width,
@@ -325,6 +505,32 @@ attn_status launch_row_softmax(const float *x, float *y, float *lse, int64_t row
     if (vec4 && width <= 4096) return rsm::launch_stream<256, 4>(x, y, lse, rows, width, ctx);
     if (vec4 && width <= rsm::kStreamMaxWidth)
         return rsm::launch_stream<512, 6>(x, y, lse, rows, width, ctx);
+    // Longer aligned rows, too few of them for one CTA per row to fill the
+    // GPU (two per SM): a cluster of CL CTAs per row, every slice at least
+    // 8192 floats.
+    const int64_t slots = 2 * (int64_t)ctx.sm_count;
+    if (vec4 && rows < slots && width <= INT32_MAX) {
+        int64_t cl = (slots + rows - 1) / rows;
+        if (cl > rsm::CL_MAX) cl = rsm::CL_MAX;
+        while (cl > 1 && width / cl < 8192) --cl;
+        if (cl > 1) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(rows * cl));
+            cfg.blockDim = dim3(rsm::CL_THREADS);
+            cfg.stream = ctx.stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)cl;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return check_launch(cudaLaunchKernelEx(&cfg, rsm::row_softmax_cluster_kernel, x, y,
+                                                   lse, rows, (int)width, (int)cl, ctx.status,
+                                                   ctx.timeout_ns),
+                                ATTN_ERR_LAUNCH);
+        }
+    }
     const int64_t max_grid = (int64_t)ctx.sm_count * 4;
     const unsigned grid = (unsigned)(rows < max_grid ? rows : max_grid);
     rsm::row_softmax_kernel<<<grid, rsm::NUM_THREADS, 0, ctx.stream>>>(x, y, lse, rows, width,

@@ -169,7 +169,9 @@ attn_status attn_fwd_host(const void *q, const void *k, const void *v, void *o, 
  *   lse   [rows] fp32 natural-log log-sum-exp per row, or NULL.
  *   rows, width >= 1, rows*width < 2^62.  Any width is accepted.
  *   -inf entries get probability 0; a row of -inf only gets all zeros and
- *   LSE = -inf.
+ *   LSE = -inf.  A few very long rows (more than 12288 floats, fewer rows than twice
+ *   the SM count, 16-byte aligned) are split over a thread-block cluster of
+ *   up to 8 CTAs per row.
  * Returns ATTN_OK or a validation / launch error (as attn_fwd).
  */
 attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,

@@ -49,11 +49,12 @@ def test_bounded_wait_times_out_and_context_survives():
 
 
 # Widths that are multiples of 4 up to 12288 take the streamed kernel (many
-# rows per CTA cycle through its 2-8 buffers and their phases); the others the
-# general one.
+# rows per CTA cycle through its two buffers and their phases); longer aligned
+# rows, when there are few of them, a cluster of CTAs per row ((2, 70000) and
+# (8, 1048576): 8 CTAs per row); the others the general kernel.
 @pytest.mark.parametrize("rows,width", [(1, 1), (3, 5), (64, 1000), (8, 11264), (4, 11265),
                                         (2, 70000), (3000, 4096), (12000, 1024), (700, 12288),
-                                        (2500, 8192), (50, 12292), (9000, 4)])
+                                        (2500, 8192), (50, 12292), (9000, 4), (8, 1048576)])
 def test_row_softmax_parity(rows, width):
     """Row softmax (any width, including rows past 65536) against the oracle."""
     x = make_rows(rows, width, seed=rows + width, spread=6.0)
@@ -81,10 +82,10 @@ def test_row_softmax_masked_and_in_place_both_paths(rows, width):
     assert np.all(np.abs(yd - y_ref) <= 1e-5 * np.abs(y_ref) + 1e-12)
 
 
-@pytest.mark.parametrize("width", [513, 512, 20000])
-def test_row_softmax_fully_masked_row(width):
-    """A row of -inf only: every probability 0 and LSE = -inf; other rows unaffected."""
-    n = 3000
+@pytest.mark.parametrize("width,n", [(513, 3000), (512, 3000), (20000, 3000), (70000, 8)])
+def test_row_softmax_fully_masked_row(width, n):
+    """A row of -inf only: every probability 0 and LSE = -inf; other rows
+    unaffected (the last case runs on the cluster kernel)."""
     x = make_rows(n, width, seed=width, spread=3.0)
     x[7] = float("-inf")
     x[n - 1] = float("-inf")
