@@ -156,7 +156,7 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                   scale: Optional[float] = None, causal: bool = False,
                   device: Optional[torch.device] = None,
                   stream: Optional[torch.cuda.Stream] = None,
-                  buffers: Optional[dict] = None
+                  buffers: Optional[dict] = None, wait: bool = True
                   ) -> Tuple[torch.Tensor, torch.Tensor]:
     """End-to-end call from host memory through the C ABI's attn_fwd_host: Q,
     K, V are copied to the device, the forward runs and O, LSE are copied back,
@@ -165,7 +165,12 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     q, k, v: contiguous CPU tensors [B, H, N, d] (pinned memory lets the copies
     overlap).  ``buffers`` may carry the reusable device workspace and pinned
     host outputs (keys ws, o_host, lse_host) so repeated calls do not allocate.
-    Returns CPU (O, LSE); the call returns after the result is on the host.
+    Returns CPU (O, LSE).  With ``wait`` (the default) the call returns after
+    the result is on the host.  With ``wait=False`` it returns once the work is
+    enqueued on ``stream``: synchronise that stream before reading the result
+    or reusing ``buffers``.  Two calls on different streams with different
+    ``buffers`` then overlap (the second one's copy in runs during the first
+    one's forward and copy out).
     """
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
@@ -200,7 +205,8 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                  lh.data_ptr(), B, H, N, d, scale, 1 if causal else 0, code,
                                  ws.data_ptr(), nbytes, _stream_handle(s, device))
         _check(st, "attn_fwd_host")
-        s.synchronize()
+        if wait:
+            s.synchronize()
     return oh, lh
 
 
