@@ -168,7 +168,9 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     Returns CPU (O, LSE).  With ``wait`` (the default) the call returns after
     the result is on the host.  With ``wait=False`` it returns once the work is
     enqueued on ``stream``: synchronise that stream before reading the result
-    or reusing ``buffers``.  Two calls on different streams with different
+    or reusing ``buffers``, and keep q, k, v alive and unchanged until then
+    (the copies read them after the call has returned; a pinned temporary
+    freed early may be reused by PyTorch's host allocator).  Two calls on different streams with different
     ``buffers`` then overlap (the second one's copy in runs during the first
     one's forward and copy out).
     """

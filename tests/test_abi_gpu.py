@@ -171,3 +171,33 @@ def test_fwd_host_pageable_inputs_and_no_lse():
     s.synchronize()
     assert device_status() == 0
     assert torch.equal(o_h, o_dev.cpu())
+
+
+def test_fwd_host_two_calls_in_flight():
+    """wait=False: two calls on two streams with their own buffers overlap, and
+    each returns exactly what a waiting call returns."""
+    B, H, N, d = 2, 8, 2048, 128
+    # Pinned inputs held for the whole test: a call that does not wait still
+    # reads them after it returns.
+    probs = [tuple(t.pin_memory() for t in make_qkv(B, H, N, d, seed=s, dtype="bf16"))
+             for s in (21, 22, 23, 24)]
+    ref = [attn_fwd_host(*p, causal=True) for p in probs]
+    ref = [(o.clone(), l.clone()) for o, l in ref]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    bufs = [{}, {}]
+    outs = []
+    for i, p in enumerate(probs):
+        if i >= 2:
+            streams[i % 2].synchronize()
+            outs.append(tuple(t.clone() for t in last[i % 2]))
+        res = attn_fwd_host(*p, causal=True, stream=streams[i % 2], buffers=bufs[i % 2],
+                            wait=False)
+        if i < 2:
+            last = [None, None] if i == 0 else last
+        last[i % 2] = res
+    for st in streams:
+        st.synchronize()
+    outs += [tuple(t.clone() for t in last[0]), tuple(t.clone() for t in last[1])]
+    assert device_status() == 0
+    for (o, l), (o_r, l_r) in zip(outs, ref):
+        assert torch.equal(o, o_r) and torch.equal(l, l_r)
