@@ -197,7 +197,9 @@ def run_reference(args, w):
     if rank != 0:
         return
     q, k, v = make_workload_inputs(w)
-    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    # About a minute of oracle work for short runs (2 s per step at most), and
+    # 0.5 s per step for long ones, so a 200-step run ends in about two minutes.
+    per_step = min(2.0, max(0.5, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(w, q, k, v, min(per_step, 2.0))
     vals, samples = [], []
