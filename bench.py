@@ -251,7 +251,7 @@ def launches_per_call(w, sms: int) -> int:
     return int(n_items - n_split > 0) + int(n_split > 0)
 
 
-EAGER_MAX_SCORE_BYTES = 8 << 30
+EAGER_MAX_SCORE_BYTES = 64 << 30  # S alone; S and P together at most 128 GiB
 
 
 def eager_context(w, qd, kd, vd, our_ms: float, our_extra: int, dev, reps: int = 5):
