@@ -155,14 +155,6 @@ __global__ void __launch_bounds__(NT)
 
 constexpr uint32_t ST_HDR = 256;  // two barriers, abort flag, reduction scratch
 
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                              uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 template <typename T>
 __device__ __forceinline__ void load8s(const uint8_t *p, float (&v)[8]) {
     load8(reinterpret_cast<const T *>(p), v);

@@ -180,14 +180,6 @@ constexpr int NS = 2;
 constexpr uint32_t ST_HDR = 256;  // NS barriers, abort flag, reduction scratch
 constexpr int64_t kStreamMaxWidth = 12288;
 
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                              uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))

@@ -155,6 +155,17 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 }
 
 // Bring one box of a tensor map into L2 (no shared memory, no barrier).
+// Untiled bulk copy of `bytes` (a multiple of 16) from global memory to this
+// CTA's shared memory, completing on mbarrier `bar` (both addresses 16-byte
+// aligned).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(tmap)),
