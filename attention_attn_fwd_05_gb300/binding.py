@@ -23,8 +23,9 @@ STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_DTYPE",
     4: "ATTN_ERR_HEADDIM", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_ARCH", 7: "ATTN_ERR_LAUNCH",
     8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
+    11: "ATTN_ERR_SCALE",
 }
-EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
+EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_fwd_noalloc_status", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
             "attn_bwd", "attn_row_softmax", "attn_add_rmsnorm", "attn_device_status",
             "attn_selftest_wait_timeout", "attn_last_cuda_error", "attn_status_string",
             "attn_version")
@@ -69,6 +70,7 @@ def lib():
         L.attn_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_float,
                                        ctypes.c_int, vp]
         L.attn_device_status.argtypes = [vp]
+        L.attn_fwd_noalloc_status.argtypes = [vp]
         L.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         L.attn_last_cuda_error.argtypes = []
         L.attn_last_cuda_error.restype = ctypes.c_char_p
@@ -78,7 +80,7 @@ def lib():
         for name in ("attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_bwd",
                      "attn_row_softmax",
                      "attn_add_rmsnorm",
-                     "attn_device_status",
+                     "attn_device_status", "attn_fwd_noalloc_status",
                      "attn_selftest_wait_timeout", "attn_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L

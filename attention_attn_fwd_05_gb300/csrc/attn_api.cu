@@ -6,6 +6,7 @@
 // "14. Triton and kernel fusion", the ValueError checks of its wrappers) --
 // but an invalid call returns an error code instead of routing elsewhere:
 // there is no fallback path.
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -43,25 +44,35 @@ attn_status device_state(DeviceState **out) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState &s = g_dev[dev];
-    if (!s.ready) {
-        s.ready = true;
-        s.init_status = ATTN_ERR_CUDA;
-        if (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) ==
-                cudaSuccess &&
-            cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev) ==
-                cudaSuccess &&
-            cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) ==
-                cudaSuccess) {
-            if (s.cc_major != 10 || s.cc_minor != 3) {
-                s.init_status = ATTN_ERR_ARCH;
-            } else if (cudaMalloc(reinterpret_cast<void **>(&s.status), 256) == cudaSuccess &&
-                       cudaMemset(s.status, 0, 256) == cudaSuccess) {
-                s.init_status = ATTN_OK;
-            }
-        }
-    }
     *out = &s;
-    return s.init_status;
+    if (s.ready) return s.init_status;
+    // Only a settled answer is cached (success, or a device of the wrong
+    // architecture); a failed runtime call, for example one made while a
+    // stream is being captured, is retried on the next call.
+    int sm_count = 0, major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    s.sm_count = sm_count;
+    s.cc_major = major;
+    s.cc_minor = minor;
+    if (major != 10 || minor != 3) {
+        s.ready = true;
+        s.init_status = ATTN_ERR_ARCH;
+        return s.init_status;
+    }
+    uint32_t *word = nullptr;
+    if (check_launch(cudaMalloc(reinterpret_cast<void **>(&word), 256), ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    if (check_launch(cudaMemset(word, 0, 256), ATTN_ERR_CUDA) != ATTN_OK) {
+        (void)cudaFree(word);
+        return ATTN_ERR_CUDA;
+    }
+    s.status = word;
+    s.init_status = ATTN_OK;
+    s.ready = true;
+    return ATTN_OK;
 }
 
 // A device pointer usable by kernels on the current device.
@@ -126,6 +137,13 @@ attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtyp
     return ATTN_OK;
 }
 
+// The softmax multiplier: any finite value.  Beyond about 2.3e38 its base-2
+// form (scale * log2 e), which the kernels use, would overflow, so those are
+// rejected with NaN and the infinities.
+attn_status check_scale(float scale) {
+    return std::fabs(scale) <= 2.0e38f ? ATTN_OK : ATTN_ERR_SCALE;
+}
+
 }  // namespace attn
 
 extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -133,7 +151,7 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
                                 int causal, int dtype, void *stream) {
     if (!q || !k || !v || !o) return ATTN_ERR_NULL;
     attn_status st = check_fwd_shape(B, H, N, d, dtype);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK || (st = check_scale(scale)) != ATTN_OK) return st;
     const int64_t BH = B * H;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_ALIGN;
@@ -191,7 +209,7 @@ extern "C" attn_status attn_fwd_host(const void *q, const void *k, const void *v
                                      size_t workspace_bytes, void *stream) {
     if (!q || !k || !v || !o || !workspace) return ATTN_ERR_NULL;
     attn_status st = check_fwd_shape(B, H, N, d, dtype);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK || (st = check_scale(scale)) != ATTN_OK) return st;
     const HostLayout lay = host_layout(B, H, N, d, dtype);
     if (workspace_bytes < lay.total) return ATTN_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
@@ -296,6 +314,7 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
     if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_DTYPE;
     if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
     if (B * H > 65535) return ATTN_ERR_SHAPE;
+    if (check_scale(scale) != ATTN_OK) return ATTN_ERR_SCALE;
     for (const void *p : {q, k, v, o, dout, static_cast<const void *>(lse),
                           static_cast<const void *>(delta), static_cast<const void *>(dq),
                           static_cast<const void *>(dk), static_cast<const void *>(dv)})
@@ -371,6 +390,7 @@ extern "C" const char *attn_status_string(int status) {
         case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (device timeout)";
         case ATTN_ERR_NOT_DEVICE: return "pointer is not device memory of the current device";
         case ATTN_ERR_CUDA: return "CUDA runtime call failed";
+        case ATTN_ERR_SCALE: return "scale is not finite (or |scale| > 2e38)";
         default: return "unknown status";
     }
 }
@@ -379,4 +399,4 @@ extern "C" const char *attn_last_cuda_error(void) {
     return cudaGetErrorString(t_last_error);
 }
 
-extern "C" int attn_version(void) { return 10100; }
+extern "C" int attn_version(void) { return 10200; }

@@ -177,8 +177,9 @@ __device__ __forceinline__ void softmax_warpgroup(
             for (int c = 0; c < BN; ++c)
                 if (key0 + c >= limit) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
         }
-        // Row max of the raw logits (scale > 0 commutes with max): 8
-        // independent 3-input chains, then a short combine.
+        // Row max of the raw logits (scale_log2 > 0 commutes with max; the
+        // launcher folds a negative scale into the S MMA): 8 independent
+        // 3-input chains, then a short combine.
         float mx8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i >> 1][(i & 1) * 16]);
@@ -296,7 +297,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const __grid_constant__ CUtensorMap tmV,
                             const __grid_constant__ CUtensorMap tmO, float *__restrict__ lse,
                             int N, int BH, int num_cta_tiles, float scale_log2, int causal,
-                            uint32_t *status, uint64_t timeout_ns, int num_sms, int GH) {
+                            uint32_t idesc_s, uint32_t *status, uint64_t timeout_ns, int num_sms,
+                            int GH) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -412,7 +414,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == WARP_MMA) {
         // ----------------------------------------------------------- MMA ---
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
             // Slot and phase of load n (K_j is load 2j, V_j is load 2j+1).
             auto slot_addr = [&](int n) -> uint32_t { return sKV + (n % C::NSLOT) * C::SLOT_BYTES; };
@@ -686,8 +687,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                   const __grid_constant__ CUtensorMap tmV,
                                   const __grid_constant__ CUtensorMap tmO,
                                   float *__restrict__ lse, int N, int BH, int num_cta_tiles,
-                                  int first_item, float scale_log2, int causal, uint32_t *status,
-                                  uint64_t timeout_ns) {
+                                  int first_item, float scale_log2, int causal, uint32_t idesc_s,
+                                  uint32_t *status, uint64_t timeout_ns) {
     using C = Cfg<D>;
     constexpr int NS = C::NSLOT + 1;
     extern __shared__ uint8_t smem_raw[];
@@ -766,7 +767,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
             auto wait_full = [&](int n) -> bool {
                 return bounded_wait(bar(C::B_FULL + n % NS), (n / NS) & 1, ctl);
@@ -945,11 +945,23 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
     if (gh64 < 1) gh64 = 1;
     if (gh64 > BH || n_split > 0) gh64 = BH;
     const int gh = (int)gh64;
-    const float scale_log2 = scale * 1.44269504088896340736f;
+    // The softmax takes each row's maximum of the raw logits and multiplies it
+    // by scale_log2, which is the maximum of the scaled logits only for a
+    // positive multiplier.  A negative scale is therefore folded into the
+    // product: the S MMA negates its A operand (instruction-descriptor bit 13),
+    // giving exactly -(Q K^T) (a sign flip of bf16 operands rounds like the
+    // original), and the kernel runs with |scale|.  A zero scale runs as the
+    // smallest normal float: masked logits (-inf) then still scale to -inf
+    // instead of -inf * 0 = NaN, and every visible scaled logit is below
+    // 2^-100 in magnitude, so each weight rounds to exp2(0) = 1 as with 0.
+    const bool negate_qk = scale < 0.f;
+    const float abs_scale = fmaxf(fabsf(scale), 1.17549435e-38f);
+    const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false) | (negate_qk ? (1u << 13) : 0u);
+    const float scale_log2 = abs_scale * 1.44269504088896340736f;
     if (n_main > 0) {
         attn_fwd_bf16_tc_kernel<D><<<(unsigned)n_main, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
             tq, tk, tv, to, lse, (int)N, (int)BH, num_cta_tiles, scale_log2, causal ? 1 : 0,
-            ctx.status, ctx.timeout_ns, ctx.sm_count, gh);
+            idesc_s, ctx.status, ctx.timeout_ns, ctx.sm_count, gh);
         const attn_status st = check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
         if (st != ATTN_OK) return st;
     }
@@ -967,7 +979,7 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
         return check_launch(cudaLaunchKernelEx(&cfg, attn_fwd_bf16_tc_split_kernel<D>, tq, tk, tv,
                                                to, lse, (int)N, (int)BH, num_cta_tiles,
                                                (int)n_main, scale_log2, causal ? 1 : 0,
-                                               ctx.status, ctx.timeout_ns),
+                                               idesc_s, ctx.status, ctx.timeout_ns),
                             ATTN_ERR_LAUNCH);
     }
     return ATTN_OK;

@@ -63,11 +63,18 @@ attn_status launch_wait_selftest(const LaunchCtx &ctx);
 // `on_error`, else ATTN_OK.  Used right after every launch.
 attn_status check_launch(cudaError_t e, attn_status on_error);
 
-// Largest N the bf16 kernel's grid can cover (query tiles on grid.y).
+// Largest N the bf16 path accepts.  The kernels' grids are 1-D (the items
+// are counted by the B*H*ceil(N/256) < 2^31 rule of check_fwd_shape); this
+// cap on N itself is kept from the first release so the documented limit
+// does not change.
 constexpr int64_t kMaxNBf16 = 65535LL * 128;
 
 // Shape, dtype and head-dim rules of attn_fwd (ATTN_OK or the error code),
 // shared by attn_fwd, attn_fwd_noalloc and attn_fwd_host.
 attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtype);
+
+// ATTN_OK for a usable softmax multiplier (finite, |scale| <= 2e38), else
+// ATTN_ERR_SCALE.  Shared by every entry point that takes a scale.
+attn_status check_scale(float scale);
 
 }  // namespace attn

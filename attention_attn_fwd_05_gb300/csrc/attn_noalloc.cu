@@ -48,28 +48,30 @@ attn_status noalloc_setup(NoAllocDevice **out) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_na_mu);
     NoAllocDevice &s = g_na[dev];
-    if (!s.ready) {
-        s.ready = true;
-        s.status = ATTN_ERR_CUDA;
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) ==
-                cudaSuccess &&
-            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ==
-                cudaSuccess &&
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ==
-                cudaSuccess) {
-            if (major != 10 || minor != 3) {
-                s.status = ATTN_ERR_ARCH;
-            } else {
-                const cudaError_t e =
-                    cudaGetSymbolAddress(reinterpret_cast<void **>(&s.scratch), g_noalloc_scratch);
-                s.status = check_launch(e, ATTN_ERR_CUDA);
-                if (s.status != ATTN_OK) s.scratch = nullptr;
-            }
-        }
-    }
     *out = &s;
-    return s.status;
+    if (s.ready) return s.status;
+    // Only a settled answer is cached (success, or a device of the wrong
+    // architecture); a failed runtime call, for example one made while a
+    // stream is being captured, is retried on the next call.
+    int sm_count = 0, major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+        s.ready = true;
+        s.status = ATTN_ERR_ARCH;
+        return s.status;
+    }
+    uint32_t *addr = nullptr;
+    if (check_launch(cudaGetSymbolAddress(reinterpret_cast<void **>(&addr), g_noalloc_scratch),
+                     ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    s.sm_count = sm_count;
+    s.scratch = addr;
+    s.status = ATTN_OK;
+    s.ready = true;
+    return ATTN_OK;
 }
 
 bool is_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -98,7 +100,7 @@ extern "C" attn_status attn_fwd_noalloc(const void *q, const void *k, const void
     // The same argument rules as attn_fwd.
     if (!q || !k || !v || !o) return ATTN_ERR_NULL;
     attn_status st = check_fwd_shape(B, H, N, d, dtype);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK || (st = check_scale(scale)) != ATTN_OK) return st;
     const int64_t BH = B * H;
     if (!is_aligned16(q) || !is_aligned16(k) || !is_aligned16(v) || !is_aligned16(o) ||
         !is_aligned16(lse))
@@ -120,4 +122,21 @@ extern "C" attn_status attn_fwd_noalloc(const void *q, const void *k, const void
     return launch_attn_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                                static_cast<const float *>(v), static_cast<float *>(o), lse, BH, N,
                                (int)d, scale, causal != 0, ctx);
+}
+
+extern "C" attn_status attn_fwd_noalloc_status(void *stream) {
+    NoAllocDevice *s = nullptr;
+    attn_status st = noalloc_setup(&s);
+    if (st != ATTN_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // Read the word into host stack memory and clear it, in stream order after
+    // the calls to be checked; nothing here allocates.
+    uint32_t word = 0;
+    if (check_launch(cudaStreamSynchronize(cs), ATTN_ERR_CUDA) != ATTN_OK ||
+        check_launch(cudaMemcpyAsync(&word, s->scratch, sizeof(word), cudaMemcpyDeviceToHost, cs),
+                     ATTN_ERR_CUDA) != ATTN_OK ||
+        check_launch(cudaMemsetAsync(s->scratch, 0, sizeof(word), cs), ATTN_ERR_CUDA) != ATTN_OK ||
+        check_launch(cudaStreamSynchronize(cs), ATTN_ERR_CUDA) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    return word ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
 }

@@ -38,6 +38,7 @@ DEFAULT_WORKLOAD = "bf16_B1_H32_N16384_d128_causal"
 METRIC = "attention fwd TFLOP/s (4*B*H*N^2*d, causal halved) and % of GB300 bf16 peak"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_BF16_DENSE_TFLOPS = 2250.0  # GB300 tensor cores, dense bf16, nominal
 KERNEL_SRC = {"bf16": "attention_attn_fwd_05_gb300/csrc/attn_fwd_tc.cu",
               "f32": "attention_attn_fwd_05_gb300/csrc/attn_fwd_f32.cu"}
 KERNEL_NAME = {"bf16": "attn_fwd_bf16_tc_kernel", "f32": "attn_fwd_f32_kernel"}
@@ -84,43 +85,59 @@ def kernel_hash(dtype: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(dtype: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary for this kernel and
-    workload, or None when there is none or the kernel changed since."""
+def profiled_value(dtype: str, workload: str, key: str):
+    """A figure (``key: value`` line) from the committed ncu summary for this
+    kernel and workload, or None when there is none or the kernel changed
+    since it was captured."""
     p = os.path.join(ROOT, "profiles", f"{KERNEL_NAME[dtype]}_{workload}.md")
     if not os.path.exists(p):
         return None
     text = open(p).read()
     h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
-    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    t = re.search(key + r":\s*([0-9.eE+]+)", text)
     if not h or not t or h.group(1) != kernel_hash(dtype):
         return None
     return float(t.group(1))
 
 
-class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+def profiled_traffic(dtype: str, workload: str):
+    """DRAM bytes per launch (read + write) from the committed ncu summary."""
+    return profiled_value(dtype, workload, "traffic_bytes_per_launch")
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+
+class ClockSampler:
+    """nvidia-smi samples (every 10 ms) of SM clock, power and throttle reasons
+    around a region.  ``mark_start``/``mark_end`` bracket the timed region on
+    the host clock, so the summary can say how many samples fell inside it."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 10
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = os.path.join("/tmp", f"attn_clocks_{os.getpid()}.csv")
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=self.out, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -132,28 +149,49 @@ class ClockSampler:
                 self.proc.kill()
             self.out.close()
 
+    @staticmethod
+    def _epoch(stamp: str):
+        """nvidia-smi timestamp ('YYYY/MM/DD HH:MM:SS.mmm', local time) -> epoch s."""
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                rows.append((self._epoch(parts[0]), float(parts[2]), float(parts[3]),
+                             float(parts[4]), parts[6:10]))
             except ValueError:
                 continue
         os.remove(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        max_mhz = max(r[1] for r in rows)
-        loaded = [r for r in rows if r[2] > 200.0] or rows
+        max_mhz = max(r[2] for r in rows)
+        inside = []
+        if self.t_start is not None and self.t_end is not None:
+            inside = [r for r in rows if r[0] is not None and self.t_start <= r[0] <= self.t_end]
+        loaded = [r for r in rows if r[3] > 200.0]
+        # Clocks reported: the samples inside the timed region, else those
+        # under load, else all.
+        use = inside or loaded or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
+        reasons = sorted({names[i] for r in (inside or loaded or rows) for i, v in enumerate(r[4])
                           if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max_mhz,
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max_mhz,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "samples_in_timed_region": len(inside),
+                "timed_region_s": (self.t_end - self.t_start)
+                if self.t_start is not None and self.t_end is not None else None,
+                "period_ms": self.PERIOD_MS,
+                "basis": "timed region" if inside else ("under load" if loaded else "all")}
 
 
 # ------------------------------------------------------------- CPU oracle ---
@@ -346,6 +384,7 @@ def run_ours(args, w):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        clk.mark_start()
         t_begin.record(stream)
         for i in range(args.steps):
             if flush:
@@ -355,6 +394,7 @@ def run_ours(args, w):
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark_end()
     if world > 1:
         torch.distributed.barrier()
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -406,7 +446,12 @@ def run_ours(args, w):
                     "kernel": KERNEL_NAME["bf16"],
                     "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} "
                                    "bf16 dense (MEASURED_PEAKS.json)",
-                    "algorithmic_flops_per_launch": w.flops}
+                    "algorithmic_flops_per_launch": w.flops,
+                    # The tensor pipe's own nominal dense rate (2.25 PFLOP/s bf16)
+                    # and the ncu tensor-pipe activity of the committed capture.
+                    "frac_of_nominal_dense": kernel_tflops / NOMINAL_BF16_DENSE_TFLOPS,
+                    "ncu_tensor_pipe_active_pct": profiled_value(
+                        "bf16", w.name, "tensor_pipe_active_pct")}
     else:
         kernel_tflops = w.flops / (statistics.mean(kernel_ms) * 1e-3) / 1e12
         # fp32 FMA pipe: 152 SMs x 128 lanes x 2 FLOP x max SM clock.
@@ -432,6 +477,8 @@ def run_ours(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic", "config": config_of(w),
         "pct_of_bf16_peak": 100.0 * tflops / world / roofline["peak"]
+        if w.dtype == "bf16" else None,
+        "pct_of_nominal_bf16_dense": 100.0 * tflops / world / NOMINAL_BF16_DENSE_TFLOPS
         if w.dtype == "bf16" else None,
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -489,11 +536,13 @@ def run_memop(args):
     stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index or 0) as clk:
+        clk.mark_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark_end()
     if device_status(device=dev) != 0:
         raise RuntimeError("device status reports a timeout")
     ms = e0.elapsed_time(e1) / args.steps
@@ -535,11 +584,13 @@ def run_bwd(args, w):
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
+        clk.mark_start()
         e0.record()
         for _ in range(args.steps):
             step()
         e1.record()
         torch.cuda.synchronize(dev)
+        clk.mark_end()
     if device_status(device=dev) != 0:
         raise RuntimeError("device status reports a timeout")
     ms = e0.elapsed_time(e1) / args.steps

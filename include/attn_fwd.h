@@ -49,7 +49,8 @@ typedef enum attn_status {
     ATTN_ERR_LAUNCH = 7,         /* the kernel launch itself failed */
     ATTN_ERR_DEVICE_TIMEOUT = 8, /* a kernel's bounded wait ran out (reported by attn_device_status) */
     ATTN_ERR_NOT_DEVICE = 9,     /* a pointer is not device-accessible memory of the current device */
-    ATTN_ERR_CUDA = 10           /* a CUDA runtime call failed during set-up or status read-back */
+    ATTN_ERR_CUDA = 10,          /* a CUDA runtime call failed during set-up or status read-back */
+    ATTN_ERR_SCALE = 11          /* scale is NaN, infinite, or larger than 2e38 in magnitude */
 } attn_status;
 
 typedef enum attn_dtype {
@@ -66,10 +67,15 @@ typedef enum attn_dtype {
  *   lse      [B,H,N] fp32 output, natural-log log-sum-exp of the scaled
  *            logits of each row (device, fully overwritten), or NULL to skip.
  *   B, H, N  batch, heads, sequence length; each >= 1, N < 2^31 and
- *            B*H*N*d < 2^62.  ATTN_BF16 also needs N <= 65535*128 and
- *            B*H*ceil(N/256) < 2^31; ATTN_F32 needs B*H <= 65535.
+ *            B*H*N*d < 2^62.  ATTN_BF16 also needs N <= 8388480 (65535*128)
+ *            and B*H*ceil(N/256) < 2^31 (the kernels' 1-D grid of
+ *            256-row items); ATTN_F32 needs B*H <= 65535.
  *   d        head dimension: 64 or 128.
  *   scale    multiplier applied to Q.K before the softmax (1/sqrt(d) usually).
+ *            Any finite value with |scale| <= 2e38: positive, negative (the
+ *            softmax then favours the smallest dot products) or zero (every
+ *            visible key weighs the same).  NaN, infinities and larger values
+ *            return ATTN_ERR_SCALE.
  *   causal   0: every key is visible; non-zero: key j visible to row i iff j <= i.
  *   dtype    an attn_dtype value.
  *   stream   cudaStream_t (as void*).
@@ -107,12 +113,24 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
  *     on the GPU (different streams, no ordering between them) race on it.
  *   - A bounded-wait timeout inside the kernel ends that launch early, and its
  *     outputs are then undefined.  The timeout is recorded only in this
- *     array, not in the word attn_device_status reads.  Callers that need
- *     timeouts reported should use attn_fwd.
+ *     array, not in the word attn_device_status reads: read it with
+ *     attn_fwd_noalloc_status, which allocates nothing either.
  */
 attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                              int64_t B, int64_t H, int64_t N, int64_t d, float scale,
                              int causal, int dtype, void *stream);
+
+/*
+ * attn_fwd_noalloc_status -- synchronise `stream`, then return and clear the
+ * status word of attn_fwd_noalloc on the current device (word 0 of its static
+ * array): ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT if a kernel launched by
+ * attn_fwd_noalloc gave up a bounded wait since the word was last cleared.
+ * ATTN_ERR_CUDA if synchronising or reading back failed.  Like
+ * attn_fwd_noalloc it allocates no device memory: the word is copied into
+ * host stack memory.  Because attn_fwd_noalloc clears the word at the start
+ * of each call, read it after the call to be checked and before the next one.
+ */
+attn_status attn_fwd_noalloc_status(void *stream);
 
 /*
  * attn_fwd_host_workspace_bytes -- bytes of device workspace attn_fwd_host
@@ -195,7 +213,8 @@ attn_status attn_row_softmax(const float *x, float *y, float *lse, int64_t rows,
  *   delta              [B,H,N] fp32 workspace owned by the caller (device,
  *                      overwritten with D); the call allocates nothing.
  *   dq, dk, dv         [B,H,N,d] outputs in `dtype` (device, fully overwritten).
- *   B, H, N, d, scale, causal, dtype, stream   as attn_fwd; B*H <= 65535.
+ *   B, H, N, d, scale, causal, dtype, stream   as attn_fwd; B*H <= 65535
+ *                      (any finite scale, as attn_fwd).
  * All pointers 16-byte aligned.  Returns ATTN_OK or a validation / launch error.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,

@@ -36,10 +36,10 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    for code in range(11):
-        assert L.attn_status_string(code)
+    for code in range(12):
+        assert L.attn_status_string(code) != b"unknown status", code
     assert L.attn_status_string(999) == b"unknown status"
-    assert L.attn_version() == 10100
+    assert L.attn_version() == 10200
 
 
 # Fake, never-dereferenced addresses: validation must reject these calls
@@ -47,8 +47,32 @@ def test_status_strings_and_version(L):
 A = 0x7F0000001000
 
 
-def call(L, q=A, k=A, v=A, o=A + 0x100000, lse=None, B=1, H=1, N=128, d=64, dtype=1):
-    return L.attn_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(0.125), 0, dtype, None)
+def call(L, q=A, k=A, v=A, o=A + 0x100000, lse=None, B=1, H=1, N=128, d=64, dtype=1,
+         scale=0.125):
+    return L.attn_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), 0, dtype, None)
+
+
+BAD_SCALES = [float("nan"), float("inf"), float("-inf"), 3.0e38, -3.0e38]
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("scale", BAD_SCALES)
+def test_non_finite_scale_rejected(L, dtype, scale):
+    """The softmax multiplier must be finite (|scale| <= 2e38): ATTN_ERR_SCALE
+    from every entry point that takes one, before any CUDA call."""
+    f = ctypes.c_float(scale)
+    assert call(L, dtype=dtype, scale=scale) == 11
+    assert L.attn_fwd_noalloc(A, A, A, A + 0x100000, None, 1, 1, 128, 64, f, 0, dtype,
+                              None) == 11
+    ws = L.attn_fwd_host_workspace_bytes(1, 1, 128, 64, dtype)
+    assert L.attn_fwd_host(A, A, A, A + 0x100000, None, 1, 1, 128, 64, f, 1, dtype,
+                           A + 0x200000, ws, None) == 11
+    assert L.attn_bwd(*([A] * 10), 1, 1, 128, 64, f, 0, dtype, None) == 11
+
+
+def test_shape_errors_come_before_the_scale_check(L):
+    assert call(L, N=0, scale=float("nan")) == 2
+    assert call(L, d=96, scale=float("nan")) == 4
 
 
 def test_null_pointers_rejected(L):
@@ -156,3 +180,25 @@ def test_fwd_host_rejects_bad_arguments_on_the_host(L):
     assert host(dtype=5) == 3
     assert host(nbytes=ws_need - 1) == 2
     assert host(ws=A + 0x200080) == 5
+
+
+def test_noalloc_objects_reference_no_device_allocator(L):
+    """The object files on attn_fwd_noalloc's path (the entry point itself and
+    the two kernel launchers it calls) reference no CUDA allocation or free
+    routine.  attn_api.o, which holds attn_fwd's per-device set-up, does: the
+    check can tell them apart.  (A static check of our own build's symbol
+    tables; the GPU test in test_zz_no_alloc.py checks the device's free
+    memory.)"""
+    import subprocess
+    from attention_attn_fwd_05_gb300.build import BUILD
+    pat = re.compile(r"^(cuda|cu)(Malloc|Free|MemAlloc|MemFree|HostAlloc|MemPool|"
+                     r"MallocAsync|FreeAsync|MallocManaged|MallocPitch|Malloc3D|MallocArray)")
+
+    def alloc_refs(obj):
+        out = subprocess.run(["nm", "-u", os.path.join(BUILD, obj)], capture_output=True,
+                             text=True, check=True).stdout
+        return [ln.split()[-1] for ln in out.splitlines() if pat.match(ln.split()[-1])]
+
+    for obj in ("attn_noalloc.o", "attn_fwd_tc.o", "attn_fwd_f32.o"):
+        assert alloc_refs(obj) == [], obj
+    assert "cudaMalloc" in alloc_refs("attn_api.o")

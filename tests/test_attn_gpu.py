@@ -105,6 +105,83 @@ def test_parity_stress_logits_small(causal):
     assert_close("bf16", o, lse, o_ref, lse_ref, 1.0, "stress")
 
 
+# ------------------------------------------------ scales other than 1/sqrt(d) ---
+#
+# The bf16 kernels take each row's maximum of the raw logits and multiply it by
+# the base-2 scale, so the sign of the scale matters (a negative scale is
+# folded into the S product); a zero scale must not turn masked logits into
+# NaN.  Every path is covered: the split kernel alone (small grids), the main
+# kernel with a split tail, d = 64 and 128, both masks, plain and stress
+# (variance-16) inputs.
+
+SCALES = [0.05, 0.3, 1.0, -0.3, "-1/sqrt(d)", 0.0]
+
+
+def _resolve(scale, d):
+    if scale == "-1/sqrt(d)":
+        return -_scale(d)
+    return float(torch.tensor(scale, dtype=torch.float32))
+
+
+@pytest.mark.parametrize("scale", SCALES)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,dist", [(1, 2, 700, "stress"), (2, 40, 300, "normal")])
+def test_parity_scales_bf16(scale, d, causal, B, H, N, dist):
+    q, k, v = make_qkv(B, H, N, d, seed=3000 + N + d, dtype="bf16", dist=dist)
+    sc = _resolve(scale, d)
+    o, lse = run_gpu(q, k, v, sc, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, sc, causal)
+    assert_close("bf16", o, lse, o_ref, lse_ref, float(v.float().abs().max()),
+                 f"bf16 d={d} causal={causal} scale={sc} {B}x{H}x{N} {dist}")
+
+
+@pytest.mark.parametrize("scale", [1.0, -0.3, 0.0])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_parity_scales_f32(scale, d, causal):
+    q, k, v = make_qkv(1, 3, 333, d, seed=3100 + d, dtype="f32")
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    assert_close("f32", o, lse, o_ref, lse_ref, float(v.abs().max()),
+                 f"f32 d={d} causal={causal} scale={scale}")
+
+
+@pytest.mark.parametrize("scale", ["-1/sqrt(d)", 0.3])
+def test_parity_scales_stress_workload_size(scale):
+    """The variance-16 stress shape at full size (B=2 H=16 N=4000 d=128,
+    causal) with a negative and a larger positive scale, on sampled rows of
+    every head plus the whole last tile."""
+    w = WORKLOADS["bf16_B2_H16_N4000_d128_causal_stress"]
+    q, k, v = inputs.make_workload_inputs(w)
+    sc = _resolve(scale, w.d)
+    o, lse = run_gpu(q, k, v, sc, w.causal)
+    rng = np.random.default_rng(w.seed + 1)
+    rows = _sample_rows(w, rng)
+    BH = w.B * w.H
+    bh_idx = np.repeat(np.arange(BH), len(rows))
+    row_idx = np.tile(np.array(rows), BH)
+    tail = np.arange(w.N - 128, w.N)
+    bh_idx = np.concatenate([bh_idx, np.full(tail.shape, BH - 1)])
+    row_idx = np.concatenate([row_idx, tail])
+    o_ref, lse_ref = oracle.attn_fwd_rows(q, k, v, sc, w.causal, bh_idx, row_idx)
+    of = o.reshape(BH, w.N, w.d)[bh_idx, row_idx]
+    lf = lse.reshape(BH, w.N)[bh_idx, row_idx]
+    assert_close("bf16", of, lf, o_ref, lse_ref, 1.0, f"stress workload scale={sc}")
+
+
+def test_negative_scale_equals_negated_queries_bitwise():
+    """scale < 0 on Q equals |scale| on -Q bit for bit: the kernel folds the
+    sign into the S product, and negating bf16 operands is exact."""
+    q, k, v = make_qkv(2, 8, 1000, 128, seed=3200, dtype="bf16", dist="stress")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    sc = _scale(128)
+    o1, l1 = attn_fwd(qd, kd, vd, -sc, True)
+    o2, l2 = attn_fwd((-qd).contiguous(), kd, vd, sc, True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_lse_optional():
     q, k, v = make_qkv(1, 1, 200, 64, seed=5, dtype="bf16")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()

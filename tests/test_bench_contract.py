@@ -57,6 +57,8 @@ def test_default_arm_line():
     assert e["h2d_bytes_per_step"] == 3 * 32 * 16384 * 128 * 2
     assert e["d2h_bytes_per_step"] == 32 * 16384 * 128 * 2 + 32 * 16384 * 4
     assert d["gpu_launches"] >= d["steps"]
+    assert abs(r["frac_of_nominal_dense"] - r["achieved"] / 2250.0) < 1e-9
     c = d["clocks"]
     assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)
+    assert c["period_ms"] == 10 and isinstance(c["samples_in_timed_region"], int)
     assert d["memory"]["extra_device_bytes_per_call"] == 0

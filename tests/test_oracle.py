@@ -188,15 +188,18 @@ def test_t6_online_replay_matches_one_shot(N, d, causal):
 
 # ------------------------------------------------------ T7 brute force ---
 
-def test_t7_two_keys_sigmoid_form():
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_t7_two_keys_sigmoid_form(sign):
     """N = 2, d = 1: O = sigma(s0 - s1) v0 + sigma(s1 - s0) v1 and
-    LSE = logaddexp(s0, s1), for random small inputs."""
+    LSE = logaddexp(s0, s1), for random small inputs, with positive and with
+    negative scales (a max taken before scaling, or a dropped sign, fails the
+    negative ones)."""
     rng = np.random.default_rng(3)
     for _ in range(20):
         q = rng.standard_normal((1, 1, 2, 1)).astype(np.float32)
         k = rng.standard_normal((1, 1, 2, 1)).astype(np.float32)
         v = rng.standard_normal((1, 1, 2, 1)).astype(np.float32)
-        scale = float(rng.uniform(0.1, 2.0))
+        scale = sign * float(rng.uniform(0.1, 2.0))
         o, lse = oracle.attn_fwd(q, k, v, scale, False)
         for i in range(2):
             s0 = scale * float(q[0, 0, i, 0]) * float(k[0, 0, 0, 0])
@@ -207,19 +210,55 @@ def test_t7_two_keys_sigmoid_form():
             assert abs(lse[0, 0, i] - np.logaddexp(s0, s1)) < 1e-14
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_t2_zero_scale_averages_visible_v(causal):
+    """scale = 0: every visible key weighs the same whatever Q and K are, so
+    O_i is the mean of the visible V rows and LSE_i = ln(#visible keys)."""
+    q, k, v = _qkv(1, 2, 37, 8, 44, "stress")
+    o, lse = oracle.attn_fwd(q, k, v, 0.0, causal)
+    v64 = v.astype(np.float64)
+    for i in range(37):
+        n = i + 1 if causal else 37
+        np.testing.assert_allclose(o[:, :, i], v64[:, :, :n].mean(axis=2), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[:, :, i], math.log(n), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_negative_scale_large_logits_one_hot(causal):
+    """A negative scale favours the smallest dot product.  With logits far
+    apart the softmax is one-hot on the key of smallest q.k (among the visible
+    ones) and LSE is that scaled logit: hand-built inputs, d = 1."""
+    N = 6
+    kv = np.array([3.0, -2.0, 5.0, -4.0, 1.0, 0.5], np.float32)
+    k = kv.reshape(1, 1, N, 1)
+    q = np.full((1, 1, N, 1), 2.0, np.float32)
+    v = np.arange(N, dtype=np.float32).reshape(1, 1, N, 1) * 10
+    scale = -50.0
+    o, lse = oracle.attn_fwd(q, k, v, scale, causal)
+    for i in range(N):
+        vis = kv[: i + 1] if causal else kv
+        j = int(np.argmin(vis))  # smallest q.k with q > 0
+        assert abs(o[0, 0, i, 0] - 10.0 * j) < 1e-9
+        assert abs(lse[0, 0, i] - scale * 2.0 * float(kv[j])) < 1e-9
+
+
 # -------------------------------------------------- T8 library cross-check ---
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dist", ["normal", "stress"])
-def test_t8_matches_float64_library_sdpa(causal, dist):
+@pytest.mark.parametrize("scale", [0.25, -0.3])
+def test_t8_matches_float64_library_sdpa(causal, dist, scale):
     """An independent float64 implementation (PyTorch's math SDPA and
-    logsumexp on the CPU) agrees to 1e-12 on the same seeded inputs."""
+    logsumexp on the CPU) agrees to 1e-12 on the same seeded inputs, for a
+    positive and a negative scale.  The library routine is given |scale| and
+    -Q for a negative scale (scale*q.k = |scale|*(-q).k exactly; its own
+    causal path does not accept a negative scale)."""
     qt, kt, vt = make_qkv(2, 3, 67, 16, 18, "bf16", dist)
-    scale = 0.25
     o, lse = oracle.attn_fwd(qt, kt, vt, scale, causal)
     q64, k64, v64 = (t.to(torch.float64) for t in (qt, kt, vt))
-    ref = torch.nn.functional.scaled_dot_product_attention(q64, k64, v64, is_causal=causal,
-                                                           scale=scale)
+    qs = q64 if scale > 0 else -q64
+    ref = torch.nn.functional.scaled_dot_product_attention(qs, k64, v64, is_causal=causal,
+                                                           scale=abs(scale))
     s = scale * q64 @ k64.transpose(-1, -2)
     if causal:
         N = s.shape[-1]
