@@ -23,7 +23,7 @@ STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_DTYPE",
     4: "ATTN_ERR_HEADDIM", 5: "ATTN_ERR_ALIGN", 6: "ATTN_ERR_ARCH", 7: "ATTN_ERR_LAUNCH",
     8: "ATTN_ERR_DEVICE_TIMEOUT", 9: "ATTN_ERR_NOT_DEVICE", 10: "ATTN_ERR_CUDA",
-    11: "ATTN_ERR_SCALE",
+    11: "ATTN_ERR_SCALE", 12: "ATTN_ERR_DEVICE_BOUNDS",
 }
 EXPORTED = ("attn_fwd", "attn_fwd_noalloc", "attn_fwd_noalloc_status", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
             "attn_bwd", "attn_row_softmax", "attn_add_rmsnorm", "attn_device_status",

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attn {
 namespace {
@@ -134,6 +135,15 @@ attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtyp
         (N > kMaxNBf16 || BH > INT32_MAX || BH * ((N + 255) / 256) > INT32_MAX))
         return ATTN_ERR_SHAPE;
     if (dtype == ATTN_F32 && (BH > 65535 || (N + 31) / 32 > INT32_MAX)) return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+
+// The attn_status a non-zero device status word stands for: an out-of-range
+// access found by the bounds-checking debug build comes first (it usually
+// also leaves a wait to time out), then a timeout.
+attn_status status_from_word(uint32_t word) {
+    if (word & STATUS_BOUNDS) return ATTN_ERR_DEVICE_BOUNDS;
+    if (word & STATUS_TIMEOUT) return ATTN_ERR_DEVICE_TIMEOUT;
     return ATTN_OK;
 }
 
@@ -364,7 +374,7 @@ extern "C" attn_status attn_device_status(void *stream) {
         cudaMemsetAsync(s->status, 0, sizeof(word), cs) != cudaSuccess ||
         cudaStreamSynchronize(cs) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    return word ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+    return status_from_word(word);
 }
 
 extern "C" attn_status attn_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
@@ -391,6 +401,8 @@ extern "C" const char *attn_status_string(int status) {
         case ATTN_ERR_NOT_DEVICE: return "pointer is not device memory of the current device";
         case ATTN_ERR_CUDA: return "CUDA runtime call failed";
         case ATTN_ERR_SCALE: return "scale is not finite (or |scale| > 2e38)";
+        case ATTN_ERR_DEVICE_BOUNDS:
+            return "a kernel found an index out of range (bounds-checking build)";
         default: return "unknown status";
     }
 }

@@ -27,6 +27,7 @@
 #include <cmath>
 
 #include "attn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attn {
 namespace f32 {
@@ -71,7 +72,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(GROUP_THREADS * G, 1)
     attn_fwd_f32_kernel(const float *__restrict__ Q, const float *__restrict__ K,
                         const float *__restrict__ V, float *__restrict__ O,
-                        float *__restrict__ LSE, int N, float scale, int causal) {
+                        float *__restrict__ LSE, int N, float scale, int causal, int BH,
+                        uint32_t *status) {
     constexpr int OC = D / 64;  // float4 column groups of O per thread
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Smem<D, G> &sm = *reinterpret_cast<Smem<D, G> *>(smem_raw);
@@ -95,7 +97,8 @@ __global__ void __launch_bounds__(GROUP_THREADS * G, 1)
     auto load_tile = [&](int k0, int b) {
         for (int idx = tid; idx < BC * (D / 4); idx += GROUP_THREADS) {
             const int kr = idx / (D / 4), c4 = idx % (D / 4);
-            const bool ok = k0 + kr < N;
+            const bool ok = k0 + kr < N &&
+                            ATTN_IN_BOUNDS(bh < BH && k0 + kr >= 0 && 4 * c4 + 4 <= D, status);
             const size_t off = ok ? base + (size_t)(k0 + kr) * D + 4 * c4 : 0;
             cp_async16(&gs.k[b][kr][4 * c4], K + off, ok);
             cp_async16(&gs.v[b][kr][4 * c4], V + off, ok);
@@ -114,7 +117,8 @@ __global__ void __launch_bounds__(GROUP_THREADS * G, 1)
     for (int idx = threadIdx.x; idx < BR * (D / 4); idx += GROUP_THREADS * G) {
         const int r = idx / (D / 4), c4 = idx % (D / 4);
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row0 + r < N) x = *reinterpret_cast<const float4 *>(Q + base + (size_t)(row0 + r) * D + 4 * c4);
+        if (row0 + r < N && ATTN_IN_BOUNDS(bh < BH && 4 * c4 + 4 <= D, status))
+            x = *reinterpret_cast<const float4 *>(Q + base + (size_t)(row0 + r) * D + 4 * c4);
         *reinterpret_cast<float4 *>(&sm.q[r][4 * c4]) = x;
     }
     __syncthreads();
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(GROUP_THREADS * G, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int row = row0 + 4 * ty + i;
-            if (row >= N) continue;
+            if (row >= N || !ATTN_IN_BOUNDS(bh < BH && row >= 0, status)) continue;
             const float inv_l = 1.f / st.l[i];
 #pragma unroll
             for (int gg = 0; gg < OC; ++gg)
@@ -282,7 +286,7 @@ static attn_status launch_g(const float *q, const float *k, const float *v, floa
         return ATTN_ERR_CUDA;
     dim3 grid((unsigned)((N + BR - 1) / BR), (unsigned)BH);
     attn_fwd_f32_kernel<D, G><<<grid, GROUP_THREADS * G, smem, ctx.stream>>>(
-        q, k, v, o, lse, (int)N, scale, causal ? 1 : 0);
+        q, k, v, o, lse, (int)N, scale, causal ? 1 : 0, (int)BH, ctx.status);
     return check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
 }
 

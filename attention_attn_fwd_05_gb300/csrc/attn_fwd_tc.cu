@@ -134,9 +134,9 @@ __device__ __forceinline__ void tile_counts(int N, int cta_tile, int causal, int
 
 template <int D>
 __device__ __forceinline__ void softmax_warpgroup(
-    int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int row0, int N, int causal,
-    float scale_log2, float *__restrict__ lse, int bh, const CUtensorMap *tmO, const WaitCtl &ctl,
-    volatile uint32_t *abort_flag) {
+    int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int row0, int N, int BH,
+    int causal, float scale_log2, float *__restrict__ lse, int bh, const CUtensorMap *tmO,
+    const WaitCtl &ctl, volatile uint32_t *abort_flag) {
     using C = Cfg<D>;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -276,12 +276,14 @@ __device__ __forceinline__ void softmax_warpgroup(
                                          __uint_as_float(v[7]) * inv_l));
             }
         }
-        if (lse != nullptr && row < N)
+        if (lse != nullptr && row < N &&
+            ATTN_IN_BOUNDS(bh >= 0 && bh < BH && row >= 0, ctl.status))
             lse[(size_t)bh * (size_t)N + (size_t)row] = (m_ref + log2f(l_run)) * LN2;
     }
     fence_proxy_async_smem();
     named_bar_sync(1 + x, BM);
-    if (t == 0 && *abort_flag == 0u && tile_row0 < N) {
+    if (t == 0 && *abort_flag == 0u && tile_row0 < N &&
+        ATTN_IN_BOUNDS(bh >= 0 && bh < BH && tile_row0 >= 0, ctl.status)) {
         // The tensor map clips rows >= N, so a ragged last tile is safe.
         for (int c = 0; c < C::DBLK; ++c)
             tma_store_3d(tmO, sStage + c * (BM * 128), c * 64, tile_row0, bh);
@@ -335,16 +337,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sQ_ = sQ;
     auto load_q = [&](int x) {
         mbar_arrive_expect_tx(bar(C::B_Q + x), C::Q_BYTES);
-        for (int c = 0; c < C::DBLK; ++c)
-            tma_load_3d(sQ_ + x * C::Q_BYTES + c * (BM * 128), &tmQ, c * 64, row0 + x * BM, bh,
-                        bar(C::B_Q + x));
+        // Tile A starts inside the sequence; tile B may lie past its end (the
+        // tensor map then fills zeros).
+        if (ATTN_IN_BOUNDS(bh >= 0 && bh < BH && row0 >= 0 && row0 < N, status))
+            for (int c = 0; c < C::DBLK; ++c)
+                tma_load_3d(sQ_ + x * C::Q_BYTES + c * (BM * 128), &tmQ, c * 64, row0 + x * BM,
+                            bh, bar(C::B_Q + x));
     };
     auto load_kv = [&](int n) {  // load n of the sequence K_0, V_0, K_1, ... into slot n % NSLOT
         const int s = n % C::NSLOT;
         mbar_arrive_expect_tx(bar(C::B_FULL + s), C::SLOT_BYTES);
-        for (int c = 0; c < C::DBLK; ++c)
-            tma_load_3d(sKV + s * C::SLOT_BYTES + c * (BN * 128), (n & 1) ? &tmV : &tmK, c * 64,
-                        (n >> 1) * BN, bh, bar(C::B_FULL + s));
+        if (ATTN_IN_BOUNDS(bh >= 0 && bh < BH && n >= 0 && (n >> 1) * BN < N, status))
+            for (int c = 0; c < C::DBLK; ++c)
+                tma_load_3d(sKV + s * C::SLOT_BYTES + c * (BN * 128), (n & 1) ? &tmV : &tmK,
+                            c * 64, (n >> 1) * BN, bh, bar(C::B_FULL + s));
     };
     if (warp == WARP_TMA && lane == 0) {
         // The producer sets up the barriers itself and starts the first copies
@@ -376,7 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode(next, nbh, ntile);
             for (int x = 0; x < 2; ++x) {
                 const int r = ntile * (2 * BM) + x * BM;
-                if (r < N)
+                if (r < N && ATTN_IN_BOUNDS(nbh >= 0 && nbh < BH, status))
                     for (int c = 0; c < C::DBLK; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, r, nbh);
             }
         }
@@ -482,8 +488,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------- softmax + epilogue ---
         const int x = warp >> 2;          // 0: tile A, 1: tile B
         const int t = threadIdx.x & 127;  // row within the tile == TMEM lane
-        softmax_warpgroup<D>(x, t, warp, tmem, sbase, x ? TB : TA, row0, N, causal, scale_log2,
-                             lse, bh, &tmO, ctl, abort_flag);
+        softmax_warpgroup<D>(x, t, warp, tmem, sbase, x ? TB : TA, row0, N, BH, causal,
+                             scale_log2, lse, bh, &tmO, ctl, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -521,7 +527,7 @@ __device__ __forceinline__ uint32_t split_slot_addr(uint32_t sbase, int n) {
 template <int D>
 __device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t tmem, uint32_t sbase,
                                               float *xch, int T, int TB, int row0, int N,
-                                              int causal, float scale_log2,
+                                              int BH, int causal, float scale_log2,
                                               float *__restrict__ lse, int bh,
                                               const CUtensorMap *tmO, const WaitCtl &ctl,
                                               volatile uint32_t *abort_flag) {
@@ -667,12 +673,14 @@ __device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t t
                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
             }
         }
-        if (x == 0 && lse != nullptr && row < N)
+        if (x == 0 && lse != nullptr && row < N &&
+            ATTN_IN_BOUNDS(bh >= 0 && bh < BH && row >= 0, ctl.status))
             lse[(size_t)bh * (size_t)N + (size_t)row] = (m + log2f(l)) * LN2;
     }
     fence_proxy_async_smem();
     named_bar_sync(3, 2 * BM);
-    if (x == 0 && t == 0 && ok && *abort_flag == 0u) {
+    if (x == 0 && t == 0 && ok && *abort_flag == 0u &&
+        ATTN_IN_BOUNDS(bh >= 0 && bh < BH && row0 >= 0 && row0 < N, ctl.status)) {
         for (int c = 0; c < C::DBLK; ++c)
             tma_store_3d(tmO, sbase + C::OFF_Q + c * (BM * 128), c * 64, row0, bh);
         tma_store_commit();
@@ -717,9 +725,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int s = n % NS;
         mbar_arrive_expect_tx(bar(C::B_FULL + s), C::SLOT_BYTES);
         const uint32_t dst = split_slot_addr<D>(sbase, n);
-        for (int c = 0; c < C::DBLK; ++c)
-            tma_load_3d(dst + c * (BN * 128), (n & 1) ? &tmV : &tmK, c * 64, (n >> 1) * BN, bh,
-                        bar(C::B_FULL + s));
+        if (ATTN_IN_BOUNDS(bh >= 0 && bh < BH && n >= 0 && (n >> 1) * BN < N, status))
+            for (int c = 0; c < C::DBLK; ++c)
+                tma_load_3d(dst + c * (BN * 128), (n & 1) ? &tmV : &tmK, c * 64, (n >> 1) * BN,
+                            bh, bar(C::B_FULL + s));
     };
     if (warp == WARP_TMA && lane == 0) {
         for (int x = 0; x < 2; ++x) {
@@ -736,8 +745,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 0u;
         fence_mbar_init();
         mbar_arrive_expect_tx(bar(C::B_Q), C::Q_BYTES);
-        for (int c = 0; c < C::DBLK; ++c)
-            tma_load_3d(sQ + c * (BM * 128), &tmQ, c * 64, row0, bh, bar(C::B_Q));
+        if (ATTN_IN_BOUNDS(rank >= 0 && rank < num_cta_tiles && bh >= 0 && bh < BH, status))
+            for (int c = 0; c < C::DBLK; ++c)
+                tma_load_3d(sQ + c * (BM * 128), &tmQ, c * 64, row0, bh, bar(C::B_Q));
         load_kv(0);
         load_kv(1);
     }
@@ -831,7 +841,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // reads by then.
         split_softmax<D>(x, t, warp, tmem, sbase,
                          reinterpret_cast<float *>(smem + C::OFF_Q + C::Q_BYTES), x ? TB : TA, TB,
-                         row0, N, causal, scale_log2, lse, bh, &tmO, ctl, abort_flag);
+                         row0, N, BH, causal, scale_log2, lse, bh, &tmO, ctl, abort_flag);
     }
     tc_fence_before();
     __syncthreads();

@@ -73,6 +73,9 @@ constexpr int64_t kMaxNBf16 = 65535LL * 128;
 // shared by attn_fwd, attn_fwd_noalloc and attn_fwd_host.
 attn_status check_fwd_shape(int64_t B, int64_t H, int64_t N, int64_t d, int dtype);
 
+// The attn_status a device status word stands for (ATTN_OK when it is 0).
+attn_status status_from_word(uint32_t word);
+
 // ATTN_OK for a usable softmax multiplier (finite, |scale| <= 2e38), else
 // ATTN_ERR_SCALE.  Shared by every entry point that takes a scale.
 attn_status check_scale(float scale);

@@ -138,5 +138,5 @@ extern "C" attn_status attn_fwd_noalloc_status(void *stream) {
         check_launch(cudaMemsetAsync(s->scratch, 0, sizeof(word), cs), ATTN_ERR_CUDA) != ATTN_OK ||
         check_launch(cudaStreamSynchronize(cs), ATTN_ERR_CUDA) != ATTN_OK)
         return ATTN_ERR_CUDA;
-    return word ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+    return status_from_word(word);
 }

@@ -80,7 +80,26 @@ struct WaitCtl {
 // Status bits recorded in the device status word.
 enum : uint32_t {
     STATUS_TIMEOUT = 1u << 0,
+    STATUS_BOUNDS = 1u << 1,  // debug build only: an index or TMA coordinate out of range
 };
+
+// Bounds checks of the debug build (compiled with -DATTN_DEBUG_BOUNDS): before
+// a global access or a TMA copy the kernels test its index or coordinates
+// against the tensor's extent (B*H, N, d).  A failed test records
+// STATUS_BOUNDS in the status word and the access is skipped (a skipped TMA
+// load then leaves its barrier incomplete, and the bounded wait on it reports
+// a timeout as well); nothing traps.  In the normal build every check is the
+// constant true and costs nothing.
+#ifdef ATTN_DEBUG_BOUNDS
+static __device__ __noinline__ bool bounds_fail(uint32_t *status) {
+    atomicOr(status, STATUS_BOUNDS);
+    __threadfence();
+    return false;
+}
+#define ATTN_IN_BOUNDS(cond, status) ((cond) ? true : ::attn::bounds_fail(status))
+#else
+#define ATTN_IN_BOUNDS(cond, status) true
+#endif
 
 // Slow path of bounded_wait (kept out of line so the fast path stays a
 // single try_wait): keep polling; every 64 polls look at the abort flag, the

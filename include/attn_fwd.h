@@ -50,7 +50,10 @@ typedef enum attn_status {
     ATTN_ERR_DEVICE_TIMEOUT = 8, /* a kernel's bounded wait ran out (reported by attn_device_status) */
     ATTN_ERR_NOT_DEVICE = 9,     /* a pointer is not device-accessible memory of the current device */
     ATTN_ERR_CUDA = 10,          /* a CUDA runtime call failed during set-up or status read-back */
-    ATTN_ERR_SCALE = 11          /* scale is NaN, infinite, or larger than 2e38 in magnitude */
+    ATTN_ERR_SCALE = 11,         /* scale is NaN, infinite, or larger than 2e38 in magnitude */
+    ATTN_ERR_DEVICE_BOUNDS = 12  /* bounds-checking debug build only: a kernel found an index or
+                                    TMA coordinate out of range and skipped the access
+                                    (reported by attn_device_status) */
 } attn_status;
 
 typedef enum attn_dtype {
@@ -252,7 +255,12 @@ attn_status attn_add_rmsnorm(const void *x, const void *residual, const void *we
  * attn_device_status -- synchronise `stream`, then return and clear the
  * current device's status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT if any
  * kernel of this library gave up a bounded wait since the last read.
- * ATTN_ERR_CUDA if synchronising or reading back failed.
+ * ATTN_ERR_CUDA if synchronising or reading back failed.  In the
+ * bounds-checking debug build (the same sources compiled with
+ * -DATTN_DEBUG_BOUNDS into a library of its own) the forward kernels check
+ * every global index and TMA coordinate against B*H, N and d before use; a
+ * failed check skips the access and this call then returns
+ * ATTN_ERR_DEVICE_BOUNDS.
  */
 attn_status attn_device_status(void *stream);
 

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    for code in range(12):
+    for code in range(13):
         assert L.attn_status_string(code) != b"unknown status", code
     assert L.attn_status_string(999) == b"unknown status"
     assert L.attn_version() == 10200

@@ -213,6 +213,7 @@ def test_parity_workload(name):
     vmax = float(v.float().abs().max())
     if w.B * w.H * w.N * w.N * w.d <= 2 ** 33:
         o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.scale, w.causal)
+        _report(name, "all rows", o, lse, o_ref, lse_ref)
         assert_close(w.dtype, o, lse, o_ref, lse_ref, vmax, name)
         return
     rng = np.random.default_rng(w.seed)
@@ -226,7 +227,15 @@ def test_parity_workload(name):
     o_ref, lse_ref = oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, bh_idx, row_idx)
     of = o.reshape(BH, w.N, w.d)[bh_idx, row_idx]
     lf = lse.reshape(BH, w.N)[bh_idx, row_idx]
+    _report(name, f"{len(row_idx)} sampled rows", of, lf, o_ref, lse_ref)
     assert_close(w.dtype, of, lf, o_ref, lse_ref, vmax, name)
+
+
+def _report(name, rows, o, lse, o_ref, lse_ref):
+    """One line per workload with the measured errors (shown with pytest -s)."""
+    eo = float(np.abs(np.asarray(o, np.float64) - o_ref).max())
+    el = float(np.abs(np.asarray(lse, np.float64) - lse_ref).max())
+    print(f"\nPARITY {name} ({rows}): max|O-O*| {eo:.2e}, max|LSE-LSE*| {el:.2e}")
 
 
 @pytest.mark.parametrize("causal", [True, False])
