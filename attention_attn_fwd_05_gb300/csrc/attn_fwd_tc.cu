@@ -132,6 +132,107 @@ __device__ __forceinline__ void tile_counts(int N, int cta_tile, int causal, int
     }
 }
 
+// What one softmax step leaves for its caller: the O rescale factor, the row
+// sum of the tile's exponentials and the reference maximum they used.  The
+// caller signals P first and folds these into its running state after, off
+// the path to the MMA issuer.
+struct TileStep {
+    float alpha, rs, m_use;
+};
+
+// One key tile of the online softmax for the calling thread's row, shared by
+// every forward kernel.  S (128 fp32 columns at tS, already complete in TMEM)
+// is read, keys >= limit are masked, and against the row's reference maximum
+// m_ref (log2 units) the tile's exponentials p = 2^(s * scale_log2 - m_use)
+// are written back over the first 64 S columns as bf16 pairs (P in TMEM).
+// The reference moves only when the tile's maximum exceeds it by more than
+// RESCALE_THRESHOLD; the O row at tO is then rescaled by alpha (allowed only
+// when `rescale_o`: the P V product that last wrote O completed with S).
+// Returns after the P stores have completed (tcgen05.wait::st) and the
+// tcgen05 fence, so the caller can arrive on the P barrier.
+template <int D>
+__device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int key0, int limit,
+                                                 uint64_t scale2, float scale_log2, float m_ref,
+                                                 bool rescale_o) {
+    uint32_t r[4][32];
+    tmem_ld_32x32b_x32(tS + 0, r[0]);
+    tmem_ld_32x32b_x32(tS + 32, r[1]);
+    tmem_ld_32x32b_x32(tS + 64, r[2]);
+    tmem_ld_32x32b_x32(tS + 96, r[3]);
+    tmem_wait_ld_x32(r[0]);
+    tmem_wait_ld_x32(r[1]);
+    tmem_wait_ld_x32(r[2]);
+    tmem_wait_ld_x32(r[3]);
+
+    if (key0 + BN > limit) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+            if (key0 + c >= limit) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+    }
+    // Row max of the raw logits (scale_log2 > 0 commutes with max; the
+    // launcher folds a negative scale into the S MMA): 8 independent
+    // 3-input chains, then a short combine.
+    float mx8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i >> 1][(i & 1) * 16]);
+#pragma unroll
+    for (int c = 1; c < 16; c += 2) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int base = (i & 1) * 16;
+            mx8[i] = fmax3(mx8[i], __uint_as_float(r[i >> 1][base + c]),
+                           __uint_as_float(r[i >> 1][base + (c + 1 < 16 ? c + 1 : c)]));
+        }
+    }
+    const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                           fmaxf(mx8[6], mx8[7]));
+    const float m_new = mx * scale_log2;
+    const bool upd = m_new > m_ref + RESCALE_THRESHOLD;
+    float m_use = upd ? m_new : m_ref;
+    if (m_use == -INFINITY) m_use = 0.f;  // row fully masked so far (never for valid rows)
+    const float alpha = upd ? ex2_approx(m_ref - m_use) : 1.f;  // 0 on the first tile
+
+    // p = 2^(s * scale_log2 - m_use): one packed FMA per pair, one MUFU
+    // exp2 per element; four packed partial sums.  The packed bf16 pairs
+    // are written back over the first 64 S columns (P in TMEM).
+    const uint64_t neg_m = pack_f32x2(-m_use, -m_use);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+    uint32_t pk[2][32];
+#pragma unroll
+    for (int c = 0; c < BN; c += 2) {
+        const uint64_t sv = pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
+                                       __uint_as_float(r[c >> 5][(c & 31) + 1]));
+        float a0, a1;
+        unpack_f32x2(ffma2(sv, scale2, neg_m), a0, a1);
+        const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+        acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pack_f32x2(p0, p1));
+        pk[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
+    }
+    tmem_st_32x32b_x32(tS + 0, pk[0]);
+    tmem_st_32x32b_x32(tS + 32, pk[1]);
+    float s0, s1, s2, s3, s4, s5, s6, s7;
+    unpack_f32x2(acc[0], s0, s1);
+    unpack_f32x2(acc[1], s2, s3);
+    unpack_f32x2(acc[2], s4, s5);
+    unpack_f32x2(acc[3], s6, s7);
+    const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+
+    if (rescale_o && __any_sync(0xffffffffu, upd)) {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO + c, o);
+            tmem_wait_ld_x32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_32x32b_x32(tO + c, o);
+        }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    return TileStep{alpha, rs, m_use};
+}
+
 template <int D>
 __device__ __forceinline__ void softmax_warpgroup(
     int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int row0, int N, int BH,
@@ -161,89 +262,10 @@ __device__ __forceinline__ void softmax_warpgroup(
             if (j >= 1) mbar_arrive(bar(C::B_EMPTY + (2 * j - 1) % C::NSLOT));
         }
         tc_fence_after();
-        uint32_t r[4][32];
-        tmem_ld_32x32b_x32(tS + 0, r[0]);
-        tmem_ld_32x32b_x32(tS + 32, r[1]);
-        tmem_ld_32x32b_x32(tS + 64, r[2]);
-        tmem_ld_32x32b_x32(tS + 96, r[3]);
-        tmem_wait_ld_x32(r[0]);
-        tmem_wait_ld_x32(r[1]);
-        tmem_wait_ld_x32(r[2]);
-        tmem_wait_ld_x32(r[3]);
-
-        const int key0 = j * BN;
-        if (key0 + BN > limit) {
-#pragma unroll
-            for (int c = 0; c < BN; ++c)
-                if (key0 + c >= limit) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-        }
-        // Row max of the raw logits (scale_log2 > 0 commutes with max; the
-        // launcher folds a negative scale into the S MMA): 8 independent
-        // 3-input chains, then a short combine.
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i >> 1][(i & 1) * 16]);
-#pragma unroll
-        for (int c = 1; c < 16; c += 2) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int base = (i & 1) * 16;
-                mx8[i] = fmax3(mx8[i], __uint_as_float(r[i >> 1][base + c]),
-                               __uint_as_float(r[i >> 1][base + (c + 1 < 16 ? c + 1 : c)]));
-            }
-        }
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
-        const float m_new = mx * scale_log2;
-        const bool upd = m_new > m_ref + RESCALE_THRESHOLD;
-        float m_use = upd ? m_new : m_ref;
-        if (m_use == -INFINITY) m_use = 0.f;  // row fully masked so far (never for valid rows)
-        const float alpha = upd ? ex2_approx(m_ref - m_use) : 1.f;  // 0 on the first tile
-
-        // p = 2^(s * scale_log2 - m_use): one packed FMA per pair, one MUFU
-        // exp2 per element; four packed partial sums.  The packed bf16 pairs
-        // are written back over the first 64 S columns (P in TMEM).
-        const uint64_t neg_m = pack_f32x2(-m_use, -m_use);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-            const uint64_t sv = pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
-                                           __uint_as_float(r[c >> 5][(c & 31) + 1]));
-            float a0, a1;
-            unpack_f32x2(ffma2(sv, scale2, neg_m), a0, a1);
-            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pack_f32x2(p0, p1));
-            pk[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_32x32b_x32(tS + 0, pk[0]);
-        tmem_st_32x32b_x32(tS + 32, pk[1]);
-        float s0, s1, s2, s3, s4, s5, s6, s7;
-        unpack_f32x2(acc[0], s0, s1);
-        unpack_f32x2(acc[1], s2, s3);
-        unpack_f32x2(acc[2], s4, s5);
-        unpack_f32x2(acc[3], s6, s7);
-        const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-
-        // O_X += P_X(j-1) V_{j-1} completed before S_X(j) did (same commit),
-        // so the O row can be rescaled here without another wait.
-        if (j > 0 && __any_sync(0xffffffffu, upd)) {
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld_32x32b_x32(tO + c, o);
-                tmem_wait_ld_x32(o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st_32x32b_x32(tO + c, o);
-            }
-        }
-        tmem_wait_st();
-        tc_fence_before();
+        const TileStep st = softmax_tile<D>(tS, tO, j * BN, limit, scale2, scale_log2, m_ref, j > 0);
         mbar_arrive(bar(C::B_PFULL + x));
-        l_run = l_run * alpha + rs;
-        m_ref = m_use;
+        l_run = l_run * st.alpha + st.rs;
+        m_ref = st.m_use;
     }
     if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_ODONE + x), 0, ctl));
     if (ok) {
@@ -554,78 +576,11 @@ __device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t t
             if (j >= 1) mbar_arrive(bar(C::B_EMPTY + (e - 3) % NS));
         }
         tc_fence_after();
-        uint32_t r[4][32];
-        tmem_ld_32x32b_x32(tS + 0, r[0]);
-        tmem_ld_32x32b_x32(tS + 32, r[1]);
-        tmem_ld_32x32b_x32(tS + 64, r[2]);
-        tmem_ld_32x32b_x32(tS + 96, r[3]);
-        tmem_wait_ld_x32(r[0]);
-        tmem_wait_ld_x32(r[1]);
-        tmem_wait_ld_x32(r[2]);
-        tmem_wait_ld_x32(r[3]);
-        const int key0 = (2 * j + x) * BN;
-        if (key0 + BN > limit) {
-#pragma unroll
-            for (int c = 0; c < BN; ++c)
-                if (key0 + c >= limit) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-        }
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i >> 1][(i & 1) * 16]);
-#pragma unroll
-        for (int c = 1; c < 16; c += 2) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int base = (i & 1) * 16;
-                mx8[i] = fmax3(mx8[i], __uint_as_float(r[i >> 1][base + c]),
-                               __uint_as_float(r[i >> 1][base + (c + 1 < 16 ? c + 1 : c)]));
-            }
-        }
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
-        const float m_new = mx * scale_log2;
-        const bool upd = m_new > m_ref + RESCALE_THRESHOLD;
-        float m_use = upd ? m_new : m_ref;
-        if (m_use == -INFINITY) m_use = 0.f;
-        const float alpha = upd ? ex2_approx(m_ref - m_use) : 1.f;
-        const uint64_t neg_m = pack_f32x2(-m_use, -m_use);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-            const uint64_t sv = pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
-                                           __uint_as_float(r[c >> 5][(c & 31) + 1]));
-            float a0, a1;
-            unpack_f32x2(ffma2(sv, scale2, neg_m), a0, a1);
-            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pack_f32x2(p0, p1));
-            pk[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_32x32b_x32(tS + 0, pk[0]);
-        tmem_st_32x32b_x32(tS + 32, pk[1]);
-        float s0, s1, s2, s3, s4, s5, s6, s7;
-        unpack_f32x2(acc[0], s0, s1);
-        unpack_f32x2(acc[1], s2, s3);
-        unpack_f32x2(acc[2], s4, s5);
-        unpack_f32x2(acc[3], s6, s7);
-        const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-        if (j > 0 && __any_sync(0xffffffffu, upd)) {
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld_32x32b_x32(tO + c, o);
-                tmem_wait_ld_x32(o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st_32x32b_x32(tO + c, o);
-            }
-        }
-        tmem_wait_st();
-        tc_fence_before();
+        const TileStep st =
+            softmax_tile<D>(tS, tO, (2 * j + x) * BN, limit, scale2, scale_log2, m_ref, j > 0);
         mbar_arrive(bar(C::B_PFULL + x));
-        l_run = l_run * alpha + rs;
-        m_ref = m_use;
+        l_run = l_run * st.alpha + st.rs;
+        m_ref = st.m_use;
     }
     // Merge.  The exchange area is a ring slot (Q_B), which the other tile's
     // last O += P V may still be reading: both tiles wait until every MMA of

@@ -95,6 +95,43 @@ def test_parity_main_kernel_and_tail(d, causal, B, H, N):
                  f"bf16 d={d} causal={causal} {B}x{H}x{N}")
 
 
+# Grids of two to three waves of 256-row items on the main kernel: CTAs of
+# one SM run items of different lengths (causal) one after the other, with
+# ragged last tiles, both head dims and items of different heads.
+MULTI_WAVE_SHAPES = [(1, 200, 300), (3, 70, 257), (2, 100, 129), (1, 160, 700)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", MULTI_WAVE_SHAPES)
+def test_parity_multi_wave(d, causal, B, H, N):
+    q, k, v = make_qkv(B, H, N, d, seed=5000 + N + d + H, dtype="bf16")
+    scale = _scale(d)
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    assert_close("bf16", o, lse, o_ref, lse_ref, float(v.float().abs().max()),
+                 f"bf16 d={d} causal={causal} {B}x{H}x{N}")
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 1.0])
+def test_parity_multi_wave_scales_stress(scale):
+    q, k, v = make_qkv(1, 160, 700, 128, seed=5100, dtype="bf16", dist="stress")
+    o, lse = run_gpu(q, k, v, scale, True)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, True)
+    assert_close("bf16", o, lse, o_ref, lse_ref, 1.0, f"multi-wave stress scale={scale}")
+
+
+def test_multi_wave_deterministic_and_lse_optional():
+    q, k, v = make_qkv(2, 100, 513, 128, seed=5200, dtype="bf16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = attn_fwd(qd, kd, vd, causal=True)
+    o2, l2 = attn_fwd(qd, kd, vd, causal=True)
+    o3, l3 = attn_fwd(qd, kd, vd, causal=True, return_lse=False)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3) and l3 is None
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_parity_stress_logits_small(causal):
     """Large logits (variance-16 Q and K) on a ragged size: online-softmax stability."""
