@@ -332,58 +332,6 @@ struct ClusterSmem {
     uint32_t abort;
 };
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
-                 : "memory");
-}
-__device__ __forceinline__ void arrive_remote(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-                 ::: "memory");
-}
-// Bounded wait on a barrier that other CTAs of the cluster arrive on: gives up
-// after `timeout_ns`, or at once when a timeout is already recorded.
-__device__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, uint32_t *status,
-                                     uint64_t timeout_ns) {
-    if (try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (try_wait_cluster(bar, parity)) return true;
-        if ((n & 63u) == 0u) {
-            if (*reinterpret_cast<volatile uint32_t *>(status) & STATUS_TIMEOUT) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) {
-                atomicOr(status, STATUS_TIMEOUT);
-                __threadfence();
-                return false;
-            }
-        }
-    }
-}
-
 __global__ void __launch_bounds__(CL_THREADS)
     row_softmax_cluster_kernel(const float *x, float *y, float *__restrict__ lse, int64_t rows,
                                int width, int CL, uint32_t *status, uint64_t timeout_ns) {

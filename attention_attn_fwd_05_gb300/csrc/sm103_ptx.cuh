@@ -146,6 +146,76 @@ __device__ __forceinline__ bool bounded_wait_warp(uint32_t bar, uint32_t parity,
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// ------------------------------------------------ clusters and DSMEM ---
+//
+// Distributed shared memory between the CTAs of a thread-block cluster on
+// this GPU: a CTA maps an address of its own shared memory to the same
+// address in cluster CTA `rank` (mapa), stores there, and arrives on an
+// mbarrier there; the owner waits on its own barrier with cluster-scope
+// acquire, which makes the stores that came before the arrivals visible.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float a, float b, float c,
+                                                 float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+// Arrive on an mbarrier of a cluster CTA (address from map_shared_to_rank),
+// releasing this thread's earlier stores at cluster scope.
+__device__ __forceinline__ void arrive_remote(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Every thread of every CTA of the cluster (unbounded: only where every path
+// of every CTA reaches it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+// Bounded wait on a barrier that other CTAs of the cluster arrive on: gives up
+// after `timeout_ns`, or at once when a timeout is already recorded.
+static __device__ __noinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity,
+                                                         uint32_t *status, uint64_t timeout_ns) {
+    if (try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (try_wait_cluster(bar, parity)) return true;
+        if ((n & 63u) == 0u) {
+            if (*reinterpret_cast<volatile uint32_t *>(status) & STATUS_TIMEOUT) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                atomicOr(status, STATUS_TIMEOUT);
+                __threadfence();
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA ---
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
