@@ -94,6 +94,12 @@ struct Cfg {
     // TMEM columns: S_A, S_B (128 fp32 columns each; P overwrites the first 64
     // as bf16 pairs), O_A, O_B (D each).
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+    // At d = 64 the main kernel has a third S buffer in the free columns
+    // 384-511: S and P of the two tiles rotate through three buffers, so a
+    // tile's next S can be computed while its softmax runs (see the issuer).
+    static constexpr bool THREE_S = (D == 64);
+    static constexpr uint32_t TM_S2 = 384;
+    static_assert(!THREE_S || (TM_O1 + D <= TM_S2 && TM_S2 + BN <= 512), "TMEM budget exceeded");
     // Barrier slots (8 bytes each).
     static constexpr int B_Q = 0;     // [2] Q_A, Q_B landed
     static constexpr int B_FULL = 2;                   // [NSLOT + 1] (the split kernel's ring
@@ -102,7 +108,10 @@ struct Cfg {
     static constexpr int B_PFULL = B_SFULL + 2;      // [2]
     static constexpr int B_ODONE = B_PFULL + 2;      // [2]
     static constexpr int B_DRAIN = B_ODONE + 2;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    // Three S buffers: the issuer commits this after the last P_B V products
+    // (those no later S_A commit covers), for tile B's O rescale.
+    static constexpr int B_OPVB = B_DRAIN + 1;
+    static constexpr int NUM_BARS = B_OPVB + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
     static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
     static_assert(8 * NUM_BARS + 8 <= BAR_BYTES, "barrier area too small");
@@ -149,11 +158,15 @@ struct TileStep {
 // RESCALE_THRESHOLD; the O row at tO is then rescaled by alpha (allowed only
 // when `rescale_o`: the P V product that last wrote O completed with S).
 // Returns after the P stores have completed (tcgen05.wait::st) and the
-// tcgen05 fence, so the caller can arrive on the P barrier.
-template <int D>
+// tcgen05 fence, so the caller can arrive on the P barrier.  With WAIT_PV the
+// rescale first waits for phase pv_parity of barrier pv_bar, a commit that
+// covers the P V product that last wrote O.
+template <int D, bool WAIT_PV = false>
 __device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int key0, int limit,
                                                  uint64_t scale2, float scale_log2, float m_ref,
-                                                 bool rescale_o) {
+                                                 bool rescale_o, uint32_t pv_bar = 0,
+                                                 uint32_t pv_parity = 0,
+                                                 const WaitCtl *ctl = nullptr) {
     uint32_t r[4][32];
     tmem_ld_32x32b_x32(tS + 0, r[0]);
     tmem_ld_32x32b_x32(tS + 32, r[1]);
@@ -218,6 +231,12 @@ __device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int k
     const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
 
     if (rescale_o && __any_sync(0xffffffffu, upd)) {
+        if constexpr (WAIT_PV) {
+            // With three S buffers S(j) can complete before O += P(j-1) V has:
+            // wait for a commit that covers that product first.
+            (void)bounded_wait(pv_bar, pv_parity, *ctl);
+            tc_fence_after();
+        }
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
@@ -235,7 +254,7 @@ __device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int k
 
 template <int D>
 __device__ __forceinline__ void softmax_warpgroup(
-    int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int row0, int N, int BH,
+    int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int TA, int row0, int N, int BH,
     int causal, float scale_log2, float *__restrict__ lse, int bh, const CUtensorMap *tmO,
     const WaitCtl &ctl, volatile uint32_t *abort_flag) {
     using C = Cfg<D>;
@@ -253,6 +272,38 @@ __device__ __forceinline__ void softmax_warpgroup(
     for (int j = 0; j < T; ++j) {
         ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL + x), j & 1, ctl));
         if (!ok) break;
+        if constexpr (C::THREE_S) {
+            if (x == 1 && t == 0) {
+                // S_B(j) is complete, and with it every MMA issued before it:
+                // S_A(j) (the last reader of K_j) and O_B += P_B(j-2) V_{j-2}
+                // (the last reader of V_{j-2}; P_B(j-1) V_{j-1} comes after).
+                mbar_arrive(bar(C::B_EMPTY + (2 * j) % C::NSLOT));
+                if (j >= 2) mbar_arrive(bar(C::B_EMPTY + (2 * j - 3) % C::NSLOT));
+            }
+            tc_fence_after();
+            // S_x(j) is in buffer (2j + x) mod 3.  An O rescale waits for the
+            // commit after O_x += P_x(j-1) V: tile A's is S_B(j)'s; tile B's is
+            // S_A(j+1)'s, or after tile A's last S a commit of its own.
+            const int b3 = (2 * j + x) % 3;
+            const uint32_t tSj = tmem + lane_base + (b3 == 2 ? C::TM_S2 : b3 * 128u);
+            uint32_t pv_bar, pv_par;
+            if (x == 0) {
+                pv_bar = bar(C::B_SFULL + 1);
+                pv_par = (uint32_t)j & 1u;
+            } else if (j + 1 < TA) {
+                pv_bar = bar(C::B_SFULL + 0);
+                pv_par = (uint32_t)(j + 1) & 1u;
+            } else {
+                pv_bar = bar(C::B_OPVB);
+                pv_par = (uint32_t)(j - 1 - max(0, TA - 2)) & 1u;
+            }
+            const TileStep st = softmax_tile<D, true>(tSj, tO, j * BN, limit, scale2, scale_log2,
+                                                      m_ref, j > 0, pv_bar, pv_par, &ctl);
+            mbar_arrive(bar(C::B_PFULL + x));
+            l_run = l_run * st.alpha + st.rs;
+            m_ref = st.m_use;
+            continue;
+        }
         if (x == 1 && t == 0) {
             // S_B(j) is complete, and with it every MMA issued before it: S_A(j)
             // (the last reader of K_j) and O_B += P_B(j-1) V_{j-1} (the last
@@ -389,6 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(C::B_EMPTY + s), 1);
         }
         mbar_init(bar(C::B_DRAIN), 1);
+        mbar_init(bar(C::B_OPVB), 1);
         *abort_flag = 0u;
         fence_mbar_init();
         load_q(0);
@@ -468,6 +520,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            sdesc_sw128(sV, BN * 128, 1024), idesc_o, first ? 0u : 1u);
             };
             bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl);
+            if constexpr (C::THREE_S) {
+                // S and P of the two tiles rotate through three TMEM buffers
+                // (S_x(j) in buffer (2j + x) mod 3), so each S runs one step
+                // ahead of its tile's P V:
+                //   S_A(0), S_B(0), S_A(1), then per key tile j
+                //   O_A += P_A(j) V_j, S_B(j+1), O_B += P_B(j) V_j, S_A(j+2).
+                // S_B(j+1) reuses S_A(j)'s buffer and S_A(j+2) S_B(j)'s, each
+                // issued after the product that reads its P.  Each tile's
+                // softmax then overlaps a whole key step of tensor work.
+                auto scol = [&](int x, int j) -> uint32_t {
+                    const int b3 = (2 * j + x) % 3;
+                    return b3 == 2 ? C::TM_S2 : b3 * 128u;
+                };
+                auto s3 = [&](int x, int j) {
+                    const uint32_t sK = slot_addr(2 * j);
+                    if constexpr (D == 128)
+                        gemm_ss_k8(tmem + scol(x, j), qdesc[x], sdesc_sw128(sK, 16, 1024), idesc_s, 0u);
+                    else
+                        gemm_ss_k4(tmem + scol(x, j), qdesc[x], sdesc_sw128(sK, 16, 1024), idesc_s, 0u);
+                    mma_commit(bar(C::B_SFULL + x));
+                };
+                auto pv3 = [&](int x, int j) {
+                    gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + scol(x, j),
+                               sdesc_sw128(slot_addr(2 * j + 1), BN * 128, 1024), idesc_o,
+                               j == 0 ? 0u : 1u);
+                };
+                if (ok && (ok = wait_full(0))) {
+                    s3(0, 0);
+                    if ((ok = bounded_wait(bar(C::B_Q + 1), 0, ctl))) {
+                        s3(1, 0);
+                        if (TA > 1 && (ok = wait_full(2))) s3(0, 1);
+                    }
+                }
+                for (int j = 0; ok && j < TB; ++j) {
+                    if (j < TA) {
+                        if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl) &&
+                                   wait_full(2 * j + 1)))
+                            break;
+                        tc_fence_after();
+                        pv3(0, j);
+                        if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
+                    }
+                    if (j + 1 < TB) {
+                        if (!(ok = wait_full(2 * j + 2))) break;
+                        s3(1, j + 1);
+                    }
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl) &&
+                               wait_full(2 * j + 1)))
+                        break;
+                    tc_fence_after();
+                    pv3(1, j);
+                    if (j + 2 >= TA) mma_commit(bar(C::B_OPVB));
+                    if (j == TB - 1) mma_commit(bar(C::B_ODONE + 1));
+                    if (j + 2 < TA) {
+                        if (!(ok = wait_full(2 * j + 4))) break;
+                        s3(0, j + 2);
+                    }
+                }
+                ok = false;  // the two-buffer schedule below is skipped
+            }
             for (int j = 0; ok && j < TB; ++j) {
                 const int nK = 2 * j;
                 if (!(ok = wait_full(nK))) break;
@@ -492,7 +604,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
                 }
             }
-            if (ok) {
+            if (ok && !C::THREE_S) {
                 const int j = TB - 1, nV = 2 * j + 1;
                 ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl) && wait_full(nV);
                 if (ok) {
@@ -510,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------- softmax + epilogue ---
         const int x = warp >> 2;          // 0: tile A, 1: tile B
         const int t = threadIdx.x & 127;  // row within the tile == TMEM lane
-        softmax_warpgroup<D>(x, t, warp, tmem, sbase, x ? TB : TA, row0, N, BH, causal,
+        softmax_warpgroup<D>(x, t, warp, tmem, sbase, x ? TB : TA, TA, row0, N, BH, causal,
                              scale_log2, lse, bh, &tmO, ctl, abort_flag);
     }
     tc_fence_before();
