@@ -300,6 +300,41 @@ def test_parity_head_groups_with_partial_last_group(causal):
                  f"H=11 N=16384 causal={causal}")
 
 
+# ------------------------------------------------------ large extents ---
+
+def test_parity_long_sequence_sampled_rows():
+    """N = 131072 (d = 64, causal): row and key-tile coordinates far beyond the
+    named workloads, checked on sampled rows of both heads, the first and last
+    tiles whole."""
+    B, H, N, d = 1, 2, 131072, 64
+    q, k, v = make_qkv(B, H, N, d, seed=91, dtype="bf16")
+    scale = _scale(d)
+    o, lse = run_gpu(q, k, v, scale, True)
+    rng = np.random.default_rng(91)
+    rows = sorted({0, 1, 127, 128, 65535, 65536, N - 129, N - 128, N - 1}
+                  | set(rng.integers(0, N, size=16).tolist()))
+    bh_idx = np.repeat(np.arange(B * H), len(rows))
+    row_idx = np.tile(np.array(rows), B * H)
+    edge = np.concatenate([np.arange(0, 128), np.arange(N - 128, N)])
+    bh_idx = np.concatenate([bh_idx, np.full(edge.shape, B * H - 1)])
+    row_idx = np.concatenate([row_idx, edge])
+    o_ref, lse_ref = oracle.attn_fwd_rows(q, k, v, scale, True, bh_idx, row_idx)
+    of = o.reshape(B * H, N, d)[bh_idx, row_idx]
+    lf = lse.reshape(B * H, N)[bh_idx, row_idx]
+    assert_close("bf16", of, lf, o_ref, lse_ref, float(v.float().abs().max()), "N=131072")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_parity_many_heads(dtype):
+    """B*H = 4096 heads of 130 rows: a grid of many waves (bf16: 4096 items) and
+    the last head's ragged tile, against the oracle on every row."""
+    q, k, v = make_qkv(64, 64, 130, 64, seed=92, dtype=dtype)
+    scale = _scale(64)
+    o, lse = run_gpu(q, k, v, scale, False)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, False)
+    assert_close(dtype, o, lse, o_ref, lse_ref, float(v.float().abs().max()), f"{dtype} B*H=4096")
+
+
 # --------------------------------------------------- GPU invariances ---
 
 def test_t3g_key_shift_on_gpu():
