@@ -137,6 +137,33 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
     return bounded_wait_slow(bar, parity, ctl);
 }
 
+// A bounded wait that never suspends: polls with the non-blocking
+// mbarrier.test_wait, and every 256 polls looks at the abort flag, the status
+// word and the clock like bounded_wait_slow.  For the single MMA-issuing
+// thread, whose reaction to a completed phase is on the critical path:
+// mbarrier.try_wait may suspend the thread, and measured on GB300 it took the
+// issuer a few hundred cycles to notice that the softmax warps had arrived.
+__device__ __forceinline__ bool spin_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((n & 255u) == 0u) {
+            if (*ctl.abort) return false;
+            if (*reinterpret_cast<volatile uint32_t *>(ctl.status) & STATUS_TIMEOUT) {
+                *ctl.abort = 1u;
+                return false;
+            }
+            if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+                *ctl.abort = 1u;
+                atomicOr(ctl.status, STATUS_TIMEOUT);
+                __threadfence();
+                return false;
+            }
+        }
+    }
+}
+
 // The same wait for a whole warp: lane 0 polls, the others wait at the
 // shuffle, and every lane gets lane 0's answer.  Call from all 32 lanes.
 __device__ __forceinline__ bool bounded_wait_warp(uint32_t bar, uint32_t parity,
