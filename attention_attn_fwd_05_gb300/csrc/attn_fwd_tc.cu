@@ -73,6 +73,12 @@ constexpr int BN = 128;           // keys per tile
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr int NUM_THREADS = 320;  // 2 softmax warpgroups + TMA warp + MMA warp
+// At d = 64 each query tile has its own MMA-issuing warp (tile A: WARP_MMA,
+// tile B: WARP_MMA_B).  One thread issues at most one tcgen05.mma per about 64
+// cycles on GB300, the time a 128 x 128 x 16 MMA takes; a 128 x 64 x 16 product
+// (P V at d = 64) takes half that, so a single issuer left the tensor pipe
+// idle half of the P V time.  Two issuers reach its rate.
+constexpr int WARP_MMA_B = 10;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LN2 = 0.69314718055994530942f;
 // Rescale O only when the running max grew by more than this (log2 units):
@@ -89,17 +95,19 @@ struct Cfg {
     static constexpr uint32_t OFF_Q = 0;                       // Q_A, Q_B (O staging later)
     static constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_BYTES;    // ring
     static constexpr uint32_t OFF_BAR = OFF_KV + NSLOT * SLOT_BYTES;
-    static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + base alignment slack
-    // TMEM columns: S_A, S_B (128 fp32 columns each; P overwrites the first 64
-    // as bf16 pairs), O_A, O_B (D each).
-    static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
-    // At d = 64 the main kernel has a third S buffer in the free columns
-    // 384-511: S and P of the two tiles rotate through three buffers, so a
-    // tile's next S can be computed while its softmax runs (see the issuer).
-    static constexpr bool THREE_S = (D == 64);
-    static constexpr uint32_t TM_S2 = 384;
-    static_assert(!THREE_S || (TM_O1 + D <= TM_S2 && TM_S2 + BN <= 512), "TMEM budget exceeded");
+    // TMEM columns: S_A, S_B (128 fp32 columns each), then at d = 128 O_A,
+    // O_B (128 each) with each P written as bf16 pairs over the first 64
+    // columns of its S.  At d = 64 each tile also has a P area of its own
+    // (64 columns) and O_A, O_B take 64 each: with S and P apart, the next S
+    // of a tile can be computed as soon as its softmax has read the current
+    // one, and each tile gets its own MMA issuer (PER_TILE).
+    static constexpr bool PER_TILE = (D == 64);
+    static constexpr uint32_t TM_S0 = 0, TM_S1 = 128;
+    static constexpr uint32_t TM_P0 = PER_TILE ? 256 : TM_S0, TM_P1 = PER_TILE ? 320 : TM_S1;
+    static constexpr uint32_t TM_O0 = PER_TILE ? 384 : 256, TM_O1 = TM_O0 + D;
+    static constexpr int THREADS = PER_TILE ? NUM_THREADS + 32 : NUM_THREADS;
     // Barrier slots (8 bytes each).
     static constexpr int B_Q = 0;     // [2] Q_A, Q_B landed
     static constexpr int B_FULL = 2;                   // [NSLOT + 1] (the split kernel's ring
@@ -108,10 +116,13 @@ struct Cfg {
     static constexpr int B_PFULL = B_SFULL + 2;      // [2]
     static constexpr int B_ODONE = B_PFULL + 2;      // [2]
     static constexpr int B_DRAIN = B_ODONE + 2;
-    // Three S buffers: the issuer commits this after the last P_B V products
-    // (those no later S_A commit covers), for tile B's O rescale.
-    static constexpr int B_OPVB = B_DRAIN + 1;
-    static constexpr int NUM_BARS = B_OPVB + 1;
+    // PER_TILE: the softmax has read S_x (the issuer may overwrite it);
+    // O_x += P_x V complete (the softmax may overwrite P_x and rescale O_x);
+    // tile B's issuer drains on its own barrier.
+    static constexpr int B_SFREE = B_DRAIN + 1;   // [2]
+    static constexpr int B_PVDONE = B_SFREE + 2;  // [2]
+    static constexpr int B_DRAIN_B = B_PVDONE + 2;
+    static constexpr int NUM_BARS = B_DRAIN_B + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
     static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
     static_assert(8 * NUM_BARS + 8 <= BAR_BYTES, "barrier area too small");
@@ -153,18 +164,21 @@ struct TileStep {
 // every forward kernel.  S (128 fp32 columns at tS, already complete in TMEM)
 // is read, keys >= limit are masked, and against the row's reference maximum
 // m_ref (log2 units) the tile's exponentials p = 2^(s * scale_log2 - m_use)
-// are written back over the first 64 S columns as bf16 pairs (P in TMEM).
-// The reference moves only when the tile's maximum exceeds it by more than
-// RESCALE_THRESHOLD; the O row at tO is then rescaled by alpha (allowed only
-// when `rescale_o`: the P V product that last wrote O completed with S).
-// Returns after the P stores have completed (tcgen05.wait::st) and the
-// tcgen05 fence, so the caller can arrive on the P barrier.  With WAIT_PV the
-// rescale first waits for phase pv_parity of barrier pv_bar, a commit that
-// covers the P V product that last wrote O.
-template <int D, bool WAIT_PV = false>
-__device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int key0, int limit,
-                                                 uint64_t scale2, float scale_log2, float m_ref,
-                                                 bool rescale_o, uint32_t pv_bar = 0,
+// are written to tP as bf16 pairs (P in TMEM, 64 columns; tP == tS writes
+// them over the first 64 S columns).  The reference moves only when the
+// tile's maximum exceeds it by more than RESCALE_THRESHOLD; the O row at tO
+// is then rescaled by alpha (allowed only when `rescale_o`).  Returns after
+// the P stores have completed (tcgen05.wait::st) and the tcgen05 fence, so
+// the caller can arrive on the P barrier.
+// PER_TILE (P apart from S): once S is read, each warp arrives on sfree_bar
+// (S may then be overwritten), and before P is written (when rescale_o, i.e.
+// not on the first tile) the caller's previous P V product, which reads P and
+// writes O, is waited for: phase pv_parity of pv_bar.
+template <int D, bool PER_TILE = false>
+__device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tP, uint32_t tO, int key0,
+                                                 int limit, uint64_t scale2, float scale_log2,
+                                                 float m_ref, bool rescale_o,
+                                                 uint32_t sfree_bar = 0, uint32_t pv_bar = 0,
                                                  uint32_t pv_parity = 0,
                                                  const WaitCtl *ctl = nullptr) {
     uint32_t r[4][32];
@@ -176,6 +190,11 @@ __device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int k
     tmem_wait_ld_x32(r[1]);
     tmem_wait_ld_x32(r[2]);
     tmem_wait_ld_x32(r[3]);
+    if constexpr (PER_TILE) {
+        tc_fence_before();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(sfree_bar);
+    }
 
     if (key0 + BN > limit) {
 #pragma unroll
@@ -221,8 +240,14 @@ __device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int k
         acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pack_f32x2(p0, p1));
         pk[c >> 6][(c >> 1) & 31] = pack_bf16x2(p0, p1);
     }
-    tmem_st_32x32b_x32(tS + 0, pk[0]);
-    tmem_st_32x32b_x32(tS + 32, pk[1]);
+    if constexpr (PER_TILE) {
+        if (rescale_o) {
+            (void)bounded_wait(pv_bar, pv_parity, *ctl);
+            tc_fence_after();
+        }
+    }
+    tmem_st_32x32b_x32(tP + 0, pk[0]);
+    tmem_st_32x32b_x32(tP + 32, pk[1]);
     float s0, s1, s2, s3, s4, s5, s6, s7;
     unpack_f32x2(acc[0], s0, s1);
     unpack_f32x2(acc[1], s2, s3);
@@ -231,12 +256,6 @@ __device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int k
     const float rs = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
 
     if (rescale_o && __any_sync(0xffffffffu, upd)) {
-        if constexpr (WAIT_PV) {
-            // With three S buffers S(j) can complete before O += P(j-1) V has:
-            // wait for a commit that covers that product first.
-            (void)bounded_wait(pv_bar, pv_parity, *ctl);
-            tc_fence_after();
-        }
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
@@ -254,13 +273,14 @@ __device__ __forceinline__ TileStep softmax_tile(uint32_t tS, uint32_t tO, int k
 
 template <int D>
 __device__ __forceinline__ void softmax_warpgroup(
-    int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int TA, int row0, int N, int BH,
+    int x, int t, int warp, uint32_t tmem, uint32_t sbase, int T, int row0, int N, int BH,
     int causal, float scale_log2, float *__restrict__ lse, int bh, const CUtensorMap *tmO,
     const WaitCtl &ctl, volatile uint32_t *abort_flag) {
     using C = Cfg<D>;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x ? C::TM_S1 : C::TM_S0);
+    const uint32_t tP = tmem + lane_base + (x ? C::TM_P1 : C::TM_P0);
     const uint32_t tO = tmem + lane_base + (x ? C::TM_O1 : C::TM_O0);
     const uint32_t sStage = sbase + C::OFF_Q + x * C::Q_BYTES;  // Q_x, reused for O
     const int tile_row0 = row0 + x * BM;
@@ -272,33 +292,19 @@ __device__ __forceinline__ void softmax_warpgroup(
     for (int j = 0; j < T; ++j) {
         ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL + x), j & 1, ctl));
         if (!ok) break;
-        if constexpr (C::THREE_S) {
-            if (x == 1 && t == 0) {
-                // S_B(j) is complete, and with it every MMA issued before it:
-                // S_A(j) (the last reader of K_j) and O_B += P_B(j-2) V_{j-2}
-                // (the last reader of V_{j-2}; P_B(j-1) V_{j-1} comes after).
+        if constexpr (C::PER_TILE) {
+            if (t == 0) {
+                // S_x(j) is complete, and with it every MMA this tile's issuer
+                // sent before it: S_x(j) read K_j, and O_x += P_x(j-2) V_{j-2}
+                // came earlier.  Both tiles read every slot, so each slot
+                // takes two releases.
                 mbar_arrive(bar(C::B_EMPTY + (2 * j) % C::NSLOT));
                 if (j >= 2) mbar_arrive(bar(C::B_EMPTY + (2 * j - 3) % C::NSLOT));
             }
             tc_fence_after();
-            // S_x(j) is in buffer (2j + x) mod 3.  An O rescale waits for the
-            // commit after O_x += P_x(j-1) V: tile A's is S_B(j)'s; tile B's is
-            // S_A(j+1)'s, or after tile A's last S a commit of its own.
-            const int b3 = (2 * j + x) % 3;
-            const uint32_t tSj = tmem + lane_base + (b3 == 2 ? C::TM_S2 : b3 * 128u);
-            uint32_t pv_bar, pv_par;
-            if (x == 0) {
-                pv_bar = bar(C::B_SFULL + 1);
-                pv_par = (uint32_t)j & 1u;
-            } else if (j + 1 < TA) {
-                pv_bar = bar(C::B_SFULL + 0);
-                pv_par = (uint32_t)(j + 1) & 1u;
-            } else {
-                pv_bar = bar(C::B_OPVB);
-                pv_par = (uint32_t)(j - 1 - max(0, TA - 2)) & 1u;
-            }
-            const TileStep st = softmax_tile<D, true>(tSj, tO, j * BN, limit, scale2, scale_log2,
-                                                      m_ref, j > 0, pv_bar, pv_par, &ctl);
+            const TileStep st = softmax_tile<D, true>(
+                tS, tP, tO, j * BN, limit, scale2, scale_log2, m_ref, j > 0, bar(C::B_SFREE + x),
+                bar(C::B_PVDONE + x), (uint32_t)(j - 1) & 1u, &ctl);
             mbar_arrive(bar(C::B_PFULL + x));
             l_run = l_run * st.alpha + st.rs;
             m_ref = st.m_use;
@@ -313,7 +319,8 @@ __device__ __forceinline__ void softmax_warpgroup(
             if (j >= 1) mbar_arrive(bar(C::B_EMPTY + (2 * j - 1) % C::NSLOT));
         }
         tc_fence_after();
-        const TileStep st = softmax_tile<D>(tS, tO, j * BN, limit, scale2, scale_log2, m_ref, j > 0);
+        const TileStep st =
+            softmax_tile<D>(tS, tS, tO, j * BN, limit, scale2, scale_log2, m_ref, j > 0);
         mbar_arrive(bar(C::B_PFULL + x));
         l_run = l_run * st.alpha + st.rs;
         m_ref = st.m_use;
@@ -366,7 +373,7 @@ __device__ __forceinline__ void softmax_warpgroup(
 }
 
 template <int D>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     attn_fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
@@ -437,10 +444,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int s = 0; s < C::NSLOT; ++s) {
             mbar_init(bar(C::B_FULL + s), 1);
-            mbar_init(bar(C::B_EMPTY + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), C::PER_TILE ? 2 : 1);
         }
         mbar_init(bar(C::B_DRAIN), 1);
-        mbar_init(bar(C::B_OPVB), 1);
+        if constexpr (C::PER_TILE) {
+            for (int x = 0; x < 2; ++x) {
+                mbar_init(bar(C::B_SFREE + x), 4);  // one arrival per softmax warp
+                mbar_init(bar(C::B_PVDONE + x), 1);
+            }
+            mbar_init(bar(C::B_DRAIN_B), 1);
+        }
         *abort_flag = 0u;
         fence_mbar_init();
         load_q(0);
@@ -491,7 +504,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 drain_wait(bar(C::B_FULL + i % C::NSLOT), (i / C::NSLOT) & 1, timeout_ns);
         }
         __syncwarp();
-    } else if (warp == WARP_MMA) {
+    } else if (warp == WARP_MMA || (C::PER_TILE && warp == WARP_MMA_B)) {
         // ----------------------------------------------------------- MMA ---
         if (lane == 0) {
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
@@ -519,115 +532,95 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + (x ? C::TM_S1 : C::TM_S0),
                            sdesc_sw128(sV, BN * 128, 1024), idesc_o, first ? 0u : 1u);
             };
-            // With two S buffers (d = 128) each P V product waits first for
-            // its V tile (long landed, off the critical path) and then,
-            // spinning, for the softmax's P, so the issuer goes from "P is
-            // ready" straight to the MMAs (+0.5-3 % measured; the same at
-            // d = 64 measured 0.5-1 % slower and is not used there).
-            bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl);
-            if constexpr (C::THREE_S) {
-                // S and P of the two tiles rotate through three TMEM buffers
-                // (S_x(j) in buffer (2j + x) mod 3), so each S runs one step
-                // ahead of its tile's P V:
-                //   S_A(0), S_B(0), S_A(1), then per key tile j
-                //   O_A += P_A(j) V_j, S_B(j+1), O_B += P_B(j) V_j, S_A(j+2).
-                // S_B(j+1) reuses S_A(j)'s buffer and S_A(j+2) S_B(j)'s, each
-                // issued after the product that reads its P.  Each tile's
-                // softmax then overlaps a whole key step of tensor work.
-                auto scol = [&](int x, int j) -> uint32_t {
-                    const int b3 = (2 * j + x) % 3;
-                    return b3 == 2 ? C::TM_S2 : b3 * 128u;
-                };
-                auto s3 = [&](int x, int j) {
-                    const uint32_t sK = slot_addr(2 * j);
-                    if constexpr (D == 128)
-                        gemm_ss_k8(tmem + scol(x, j), qdesc[x], sdesc_sw128(sK, 16, 1024), idesc_s, 0u);
-                    else
-                        gemm_ss_k4(tmem + scol(x, j), qdesc[x], sdesc_sw128(sK, 16, 1024), idesc_s, 0u);
+            if constexpr (C::PER_TILE) {
+                // One issuer per tile, each with its own S, P and O, so the two
+                // never wait for each other.  Tile x's next S is issued as soon
+                // as its softmax has read the current one:
+                //   S_x(0), then per key tile j
+                //   [S read] S_x(j+1), [P_x(j) written] O_x += P_x(j) V_j.
+                const int x = warp - WARP_MMA;
+                const int T = x ? TB : TA;
+                const uint32_t tS = tmem + (x ? C::TM_S1 : C::TM_S0);
+                const uint32_t tP = tmem + (x ? C::TM_P1 : C::TM_P0);
+                const uint32_t tO = tmem + (x ? C::TM_O1 : C::TM_O0);
+                auto issue_s1 = [&](int j) {
+                    gemm_ss_k4(tS, qdesc[x], sdesc_sw128(slot_addr(2 * j), 16, 1024), idesc_s, 0u);
                     mma_commit(bar(C::B_SFULL + x));
                 };
-                auto pv3 = [&](int x, int j) {
-                    gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + scol(x, j),
-                               sdesc_sw128(slot_addr(2 * j + 1), BN * 128, 1024), idesc_o,
-                               j == 0 ? 0u : 1u);
-                };
-                if (ok && (ok = wait_full(0))) {
-                    s3(0, 0);
-                    if ((ok = bounded_wait(bar(C::B_Q + 1), 0, ctl))) {
-                        s3(1, 0);
-                        if (TA > 1 && (ok = wait_full(2))) s3(0, 1);
-                    }
-                }
-                for (int j = 0; ok && j < TB; ++j) {
-                    if (j < TA) {
-                        if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl) &&
-                                   wait_full(2 * j + 1)))
+                bool ok = bounded_wait(bar(C::B_Q + x), 0, ctl) && wait_full(0);
+                if (ok) issue_s1(0);
+                for (int j = 0; ok && j < T; ++j) {
+                    if (j + 1 < T) {
+                        if (!(ok = bounded_wait(bar(C::B_SFREE + x), j & 1, ctl) &&
+                                   wait_full(2 * j + 2)))
                             break;
                         tc_fence_after();
-                        pv3(0, j);
-                        if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
+                        issue_s1(j + 1);
                     }
-                    if (j + 1 < TB) {
-                        if (!(ok = wait_full(2 * j + 2))) break;
-                        s3(1, j + 1);
-                    }
-                    if (!(ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl) &&
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + x), j & 1, ctl) &&
                                wait_full(2 * j + 1)))
                         break;
                     tc_fence_after();
-                    pv3(1, j);
-                    if (j + 2 >= TA) mma_commit(bar(C::B_OPVB));
-                    if (j == TB - 1) mma_commit(bar(C::B_ODONE + 1));
-                    if (j + 2 < TA) {
-                        if (!(ok = wait_full(2 * j + 4))) break;
-                        s3(0, j + 2);
+                    gemm_ts_k8(tO, tP, sdesc_sw128(slot_addr(2 * j + 1), BN * 128, 1024), idesc_o,
+                               j == 0 ? 0u : 1u);
+                    mma_commit(bar(C::B_PVDONE + x));
+                    if (j == T - 1) mma_commit(bar(C::B_ODONE + x));
+                }
+                // Every MMA this thread issued must finish before TMEM is released.
+                const uint32_t drain = bar(x ? C::B_DRAIN_B : C::B_DRAIN);
+                mma_commit(drain);
+                drain_wait(drain, 0, timeout_ns);
+            } else {
+                // Two S buffers (d = 128), one issuer for both tiles.  Each P V
+                // product waits first for its V tile (long landed, off the
+                // critical path) and then, spinning, for the softmax's P, so the
+                // issuer goes from "P is ready" straight to the MMAs (+0.5-3 %
+                // measured).
+                bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl);
+                for (int j = 0; ok && j < TB; ++j) {
+                    const int nK = 2 * j;
+                    if (!(ok = wait_full(nK))) break;
+                    if (j < TA) issue_s(0, slot_addr(nK));
+                    if (j >= 1) {
+                        // O_B += P_B(j-1) V_{j-1}.
+                        const int nV = 2 * (j - 1) + 1;
+                        if (!(ok = wait_full(nV) &&
+                                   spin_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(1, slot_addr(nV), j == 1);
+                    }
+                    if (j == 0 && !(ok = bounded_wait(bar(C::B_Q + 1), 0, ctl))) break;
+                    issue_s(1, slot_addr(nK));
+                    if (j < TA) {
+                        const int nV = 2 * j + 1;
+                        if (!(ok = wait_full(nV) && spin_wait(bar(C::B_PFULL + 0), j & 1, ctl)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(0, slot_addr(nV), j == 0);
+                        if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
                     }
                 }
-                ok = false;  // the two-buffer schedule below is skipped
-            }
-            for (int j = 0; ok && j < TB; ++j) {
-                const int nK = 2 * j;
-                if (!(ok = wait_full(nK))) break;
-                if (j < TA) issue_s(0, slot_addr(nK));
-                if (j >= 1) {
-                    // O_B += P_B(j-1) V_{j-1}.
-                    const int nV = 2 * (j - 1) + 1;
-                    if (!(ok = wait_full(nV) &&
-                               spin_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl)))
-                        break;
-                    tc_fence_after();
-                    issue_pv(1, slot_addr(nV), j == 1);
-                }
-                if (j == 0 && !(ok = bounded_wait(bar(C::B_Q + 1), 0, ctl))) break;
-                issue_s(1, slot_addr(nK));
-                if (j < TA) {
-                    const int nV = 2 * j + 1;
-                    if (!(ok = wait_full(nV) && spin_wait(bar(C::B_PFULL + 0), j & 1, ctl)))
-                        break;
-                    tc_fence_after();
-                    issue_pv(0, slot_addr(nV), j == 0);
-                    if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
-                }
-            }
-            if (ok && !C::THREE_S) {
-                const int j = TB - 1, nV = 2 * j + 1;
-                ok = wait_full(nV) && spin_wait(bar(C::B_PFULL + 1), j & 1, ctl);
                 if (ok) {
-                    tc_fence_after();
-                    issue_pv(1, slot_addr(nV), j == 0);
-                    mma_commit(bar(C::B_ODONE + 1));
+                    const int j = TB - 1, nV = 2 * j + 1;
+                    ok = wait_full(nV) && spin_wait(bar(C::B_PFULL + 1), j & 1, ctl);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_pv(1, slot_addr(nV), j == 0);
+                        mma_commit(bar(C::B_ODONE + 1));
+                    }
                 }
+                // Every MMA issued above must finish before TMEM is released.
+                mma_commit(bar(C::B_DRAIN));
+                drain_wait(bar(C::B_DRAIN), 0, timeout_ns);
             }
-            // Every MMA issued above must finish before TMEM is released.
-            mma_commit(bar(C::B_DRAIN));
-            drain_wait(bar(C::B_DRAIN), 0, timeout_ns);
         }
         __syncwarp();
     } else {
         // ------------------------------------------- softmax + epilogue ---
         const int x = warp >> 2;          // 0: tile A, 1: tile B
         const int t = threadIdx.x & 127;  // row within the tile == TMEM lane
-        softmax_warpgroup<D>(x, t, warp, tmem, sbase, x ? TB : TA, TA, row0, N, BH, causal,
+        softmax_warpgroup<D>(x, t, warp, tmem, sbase, x ? TB : TA, row0, N, BH, causal,
                              scale_log2, lse, bh, &tmO, ctl, abort_flag);
     }
     tc_fence_before();
@@ -694,7 +687,7 @@ __device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t t
         }
         tc_fence_after();
         const TileStep st =
-            softmax_tile<D>(tS, tO, (2 * j + x) * BN, limit, scale2, scale_log2, m_ref, j > 0);
+            softmax_tile<D>(tS, tS, tO, (2 * j + x) * BN, limit, scale2, scale_log2, m_ref, j > 0);
         mbar_arrive(bar(C::B_PFULL + x));
         l_run = l_run * st.alpha + st.rs;
         m_ref = st.m_use;
@@ -1041,7 +1034,7 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
     const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false) | (negate_qk ? (1u << 13) : 0u);
     const float scale_log2 = abs_scale * 1.44269504088896340736f;
     if (n_main > 0) {
-        attn_fwd_bf16_tc_kernel<D><<<(unsigned)n_main, NUM_THREADS, C::SMEM_BYTES, ctx.stream>>>(
+        attn_fwd_bf16_tc_kernel<D><<<(unsigned)n_main, C::THREADS, C::SMEM_BYTES, ctx.stream>>>(
             tq, tk, tv, to, lse, (int)N, (int)BH, num_cta_tiles, scale_log2, causal ? 1 : 0,
             idesc_s, ctx.status, ctx.timeout_ns, ctx.sm_count, gh);
         const attn_status st = check_launch(cudaGetLastError(), ATTN_ERR_LAUNCH);
