@@ -56,7 +56,7 @@ class Workload:
         return 4 * n * self.elem_bytes + self.B * self.H * self.N * 4
 
 
-# The five problem shapes the method is measured and checked on.
+# The problem shapes the method is measured and checked on.
 WORKLOADS = {
     w.name: w for w in [
         Workload("f32_B1_H1_N128_d64", "f32", 1, 1, 128, 64, False, 0),
@@ -67,6 +67,8 @@ WORKLOADS = {
         Workload("bf16_B1_H32_N16384_d128_causal", "bf16", 1, 32, 16384, 128, True, 3),
         Workload("bf16_B2_H16_N4000_d128_causal_stress", "bf16", 2, 16, 4000, 128, True, 4,
                  "stress"),
+        # The long causal sequence again at head dimension 64.
+        Workload("bf16_B1_H32_N16384_d64_causal", "bf16", 1, 32, 16384, 64, True, 5),
     ]
 }
 
