@@ -637,9 +637,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 // for every item of a grid that fills at most half the SMs, two CTAs share an
 // item, one per 128-row half.  In such a CTA both query tiles hold the same
 // rows (Q is loaded once, into Q_A): tile A walks the even key tiles and tile
-// B the odd ones, with the same MMA order as the main kernel (S_A(j),
-// O_B += P_B(j-1) V, S_B(j), O_A += P_A(j) V), so the tensor core still works
-// on one tile while the other's softmax runs.  At the end the two partial
+// B the odd ones.  At d = 128 one issuer runs S_A(j), O_B += P_B(j-1) V,
+// S_B(j), O_A += P_A(j) V, so the tensor core works on one tile while the
+// other's softmax runs; at d = 64 each tile has its own issuer, S apart from
+// P, as in the main kernel.  At the end the two partial
 // results (m, l, O) of each row are merged with the online rule.  Every step
 // streams two K and two V tiles, so the ring gets one more slot: the unused
 // Q_B buffer.
@@ -668,6 +669,7 @@ __device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t t
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (x ? C::TM_S1 : C::TM_S0);
+    const uint32_t tP = tmem + lane_base + (x ? C::TM_P1 : C::TM_P0);
     const uint32_t tO = tmem + lane_base + (x ? C::TM_O1 : C::TM_O0);
     const int row = row0 + t;
     const int limit = causal ? min(N, row + 1) : N;
@@ -677,11 +679,27 @@ __device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t t
     for (int j = 0; j < T; ++j) {
         ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL + x), j & 1, ctl));
         if (!ok) break;
+        const int e = split_entry_k(x, j);
+        if constexpr (C::PER_TILE) {
+            // One issuer per tile: S_x(j) complete frees its own K tile; the V
+            // tile read in the previous step is free once the softmax has seen
+            // O_x += P_x(j-1) V complete (inside softmax_tile, before P is
+            // overwritten).
+            if (t == 0) mbar_arrive(bar(C::B_EMPTY + e % NS));
+            tc_fence_after();
+            const TileStep st = softmax_tile<D, true>(
+                tS, tP, tO, (2 * j + x) * BN, limit, scale2, scale_log2, m_ref, j > 0,
+                bar(C::B_SFREE + x), bar(C::B_PVDONE + x), (uint32_t)(j - 1) & 1u, &ctl);
+            if (t == 0 && j >= 1) mbar_arrive(bar(C::B_EMPTY + (e - 3) % NS));
+            mbar_arrive(bar(C::B_PFULL + x));
+            l_run = l_run * st.alpha + st.rs;
+            m_ref = st.m_use;
+            continue;
+        }
         if (t == 0) {
             // S_x(j) is complete, and with it every MMA issued before it: its
             // own K tile is free, and so is the V tile this tile read in the
             // previous step (O_x += P_x(j-1) V was issued before S_x(j)).
-            const int e = split_entry_k(x, j);
             mbar_arrive(bar(C::B_EMPTY + e % NS));
             if (j >= 1) mbar_arrive(bar(C::B_EMPTY + (e - 3) % NS));
         }
@@ -754,7 +772,7 @@ __device__ __forceinline__ void split_softmax(int x, int t, int warp, uint32_t t
 }
 
 template <int D>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     attn_fwd_bf16_tc_split_kernel(const __grid_constant__ CUtensorMap tmQ,
                                   const __grid_constant__ CUtensorMap tmK,
                                   const __grid_constant__ CUtensorMap tmV,
@@ -807,6 +825,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(C::B_EMPTY + s), 1);
         }
         mbar_init(bar(C::B_DRAIN), 1);
+        if constexpr (C::PER_TILE) {
+            for (int x = 0; x < 2; ++x) {
+                mbar_init(bar(C::B_SFREE + x), 4);  // one arrival per softmax warp
+                mbar_init(bar(C::B_PVDONE + x), 1);
+            }
+            mbar_init(bar(C::B_DRAIN_B), 1);
+        }
         *abort_flag = 0u;
         fence_mbar_init();
         mbar_arrive_expect_tx(bar(C::B_Q), C::Q_BYTES);
@@ -840,63 +865,103 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 drain_wait(bar(C::B_FULL + i % NS), (i / NS) & 1, timeout_ns);
         }
         __syncwarp();
-    } else if (warp == WARP_MMA) {
+    } else if (warp == WARP_MMA || (C::PER_TILE && warp == WARP_MMA_B)) {
         if (lane == 0) {
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, false, true);
             auto wait_full = [&](int n) -> bool {
                 return bounded_wait(bar(C::B_FULL + n % NS), (n / NS) & 1, ctl);
             };
             const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);  // both tiles read Q_A
-            auto issue_s = [&](int x, int n) {
-                const uint32_t dS = tmem + (x ? C::TM_S1 : C::TM_S0);
-                const uint64_t kd = sdesc_sw128(split_slot_addr<D>(sbase, n), 16, 1024);
-                if constexpr (D == 128)
-                    gemm_ss_k8(dS, qdesc, kd, idesc_s, 0u);
-                else
-                    gemm_ss_k4(dS, qdesc, kd, idesc_s, 0u);
-                mma_commit(bar(C::B_SFULL + x));
-            };
-            auto issue_pv = [&](int x, int n, bool first) {
-                gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + (x ? C::TM_S1 : C::TM_S0),
-                           sdesc_sw128(split_slot_addr<D>(sbase, n), BN * 128, 1024), idesc_o,
-                           first ? 0u : 1u);
-            };
-            bool ok = bounded_wait(bar(C::B_Q), 0, ctl);
-            for (int j = 0; ok && j < TA; ++j) {  // TA >= TB
-                const int nKA = split_entry_k(0, j), nKB = split_entry_k(1, j);
-                if (!(ok = wait_full(nKA))) break;
-                issue_s(0, nKA);
-                if (j >= 1) {
-                    // O_B += P_B(j-1) V (key tile 2j - 1).
-                    const int nV = split_entry_k(1, j - 1) + 1;
-                    if (!(ok = bounded_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl) &&
-                               wait_full(nV)))
+            if constexpr (C::PER_TILE) {
+                // d = 64: one issuer per tile, as in the main kernel (the two
+                // tiles read different key tiles, so they share nothing but Q).
+                const int x = warp - WARP_MMA;
+                const int T = x ? TB : TA;
+                const uint32_t tS = tmem + (x ? C::TM_S1 : C::TM_S0);
+                const uint32_t tP = tmem + (x ? C::TM_P1 : C::TM_P0);
+                const uint32_t tO = tmem + (x ? C::TM_O1 : C::TM_O0);
+                auto issue_s1 = [&](int j) {
+                    const uint64_t kd =
+                        sdesc_sw128(split_slot_addr<D>(sbase, split_entry_k(x, j)), 16, 1024);
+                    gemm_ss_k4(tS, qdesc, kd, idesc_s, 0u);
+                    mma_commit(bar(C::B_SFULL + x));
+                };
+                bool ok = T > 0 && bounded_wait(bar(C::B_Q), 0, ctl) &&
+                          wait_full(split_entry_k(x, 0));
+                if (ok) issue_s1(0);
+                for (int j = 0; ok && j < T; ++j) {
+                    if (j + 1 < T) {
+                        if (!(ok = bounded_wait(bar(C::B_SFREE + x), j & 1, ctl) &&
+                                   wait_full(split_entry_k(x, j + 1))))
+                            break;
+                        tc_fence_after();
+                        issue_s1(j + 1);
+                    }
+                    const int nV = split_entry_k(x, j) + 1;
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + x), j & 1, ctl) && wait_full(nV)))
                         break;
                     tc_fence_after();
-                    issue_pv(1, nV, j == 1);
-                    if (j - 1 == TB - 1) mma_commit(bar(C::B_ODONE + 1));
+                    gemm_ts_k8(tO, tP, sdesc_sw128(split_slot_addr<D>(sbase, nV), BN * 128, 1024),
+                               idesc_o, j == 0 ? 0u : 1u);
+                    mma_commit(bar(C::B_PVDONE + x));
+                    if (j == T - 1) mma_commit(bar(C::B_ODONE + x));
                 }
-                if (j < TB) {
-                    if (!(ok = wait_full(nKB))) break;
-                    issue_s(1, nKB);
-                }
-                const int nV = nKA + 1;
-                if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl) && wait_full(nV))) break;
-                tc_fence_after();
-                issue_pv(0, nV, j == 0);
-                if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
-            }
-            if (ok && TB >= 1 && TA == TB) {
-                const int j = TB - 1, nV = split_entry_k(1, j) + 1;
-                ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl) && wait_full(nV);
-                if (ok) {
+                const uint32_t drain = bar(x ? C::B_DRAIN_B : C::B_DRAIN);
+                mma_commit(drain);
+                drain_wait(drain, 0, timeout_ns);
+            } else {
+                // d = 128: one issuer for both tiles.
+                auto issue_s = [&](int x, int n) {
+                    const uint32_t dS = tmem + (x ? C::TM_S1 : C::TM_S0);
+                    const uint64_t kd = sdesc_sw128(split_slot_addr<D>(sbase, n), 16, 1024);
+                    if constexpr (D == 128)
+                        gemm_ss_k8(dS, qdesc, kd, idesc_s, 0u);
+                    else
+                        gemm_ss_k4(dS, qdesc, kd, idesc_s, 0u);
+                    mma_commit(bar(C::B_SFULL + x));
+                };
+                auto issue_pv = [&](int x, int n, bool first) {
+                    gemm_ts_k8(tmem + (x ? C::TM_O1 : C::TM_O0), tmem + (x ? C::TM_S1 : C::TM_S0),
+                               sdesc_sw128(split_slot_addr<D>(sbase, n), BN * 128, 1024), idesc_o,
+                               first ? 0u : 1u);
+                };
+                bool ok = bounded_wait(bar(C::B_Q), 0, ctl);
+                for (int j = 0; ok && j < TA; ++j) {  // TA >= TB
+                    const int nKA = split_entry_k(0, j), nKB = split_entry_k(1, j);
+                    if (!(ok = wait_full(nKA))) break;
+                    issue_s(0, nKA);
+                    if (j >= 1) {
+                        // O_B += P_B(j-1) V (key tile 2j - 1).
+                        const int nV = split_entry_k(1, j - 1) + 1;
+                        if (!(ok = bounded_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl) &&
+                                   wait_full(nV)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(1, nV, j == 1);
+                        if (j - 1 == TB - 1) mma_commit(bar(C::B_ODONE + 1));
+                    }
+                    if (j < TB) {
+                        if (!(ok = wait_full(nKB))) break;
+                        issue_s(1, nKB);
+                    }
+                    const int nV = nKA + 1;
+                    if (!(ok = bounded_wait(bar(C::B_PFULL + 0), j & 1, ctl) && wait_full(nV))) break;
                     tc_fence_after();
-                    issue_pv(1, nV, j == 0);
-                    mma_commit(bar(C::B_ODONE + 1));
+                    issue_pv(0, nV, j == 0);
+                    if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
                 }
+                if (ok && TB >= 1 && TA == TB) {
+                    const int j = TB - 1, nV = split_entry_k(1, j) + 1;
+                    ok = bounded_wait(bar(C::B_PFULL + 1), j & 1, ctl) && wait_full(nV);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_pv(1, nV, j == 0);
+                        mma_commit(bar(C::B_ODONE + 1));
+                    }
+                }
+                mma_commit(bar(C::B_DRAIN));
+                drain_wait(bar(C::B_DRAIN), 0, timeout_ns);
             }
-            mma_commit(bar(C::B_DRAIN));
-            drain_wait(bar(C::B_DRAIN), 0, timeout_ns);
         }
         __syncwarp();
     } else {
@@ -1043,7 +1108,7 @@ static attn_status launch(const void *q, const void *k, const void *v, void *o, 
     if (n_split > 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(2 * n_split));
-        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.blockDim = dim3(C::THREADS);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = ctx.stream;
         cudaLaunchAttribute attr[1];
