@@ -16,8 +16,9 @@
 //               those copies overlap the TMEM allocation; it also warms L2
 //               with the query block of the CTA that will start next.  Then
 //               K_1, V_1, K_2, ... into a ring of NSLOT shared-memory slots
-//               (128-byte swizzle, 64-column boxes).  Slots come back when
-//               tile B's softmax sees S_B(j) complete (see softmax_warpgroup).
+//               (128-byte swizzle, 64-column boxes).  Slots come back when the
+//               softmax sees S complete (see softmax_warpgroup).
+//   d = 128:
 //   warp 9      TMEM allocator and MMA issuer (one thread).  Per key tile j it
 //               issues, in this order,
 //                 S_A(j) = Q_A K_j^T,  O_B += P_B(j-1) V_{j-1},
@@ -29,17 +30,22 @@
 //               (A operand in TMEM): P never touches shared memory.  The next
 //               S of a tile is issued after that tile's P V in the MMA stream,
 //               and tcgen05 MMAs from one thread execute in issue order, so it
-//               overwrites P only after P V has read it.
+//               overwrites P only after P V has read it.  The S_X(j) commit
+//               also covers O_X += P_X(j-1) V_{j-1}, so O is complete when S
+//               is.
+//   d = 64:
+//   warps 9, 10 one MMA issuer per tile; each tile's P has TMEM columns of its
+//               own, and its next S is issued as soon as its softmax has read
+//               the current one (see the issuer).
 //   warps 0-3   softmax + epilogue of tile A, one query row per thread (TMEM
 //   warps 4-7   lane = row); same for tile B.  Per key tile: read S, mask,
 //               row max (tree), p = 2^(s*scale*log2e - m) packed to bf16 into
 //               TMEM, row sum.  The O row is rescaled only when the row max grew
 //               by more than 2^8 since the reference it was last scaled to (the
 //               reference only has to bound the exponentials; O and l always
-//               share it, so the result is unchanged).  The S_X(j) commit also
-//               covers O_X += P_X(j-1) V_{j-1}, so O is complete when S is.  At
-//               the end O / l -> bf16 -> shared (the Q buffer of the tile, no
-//               longer read) -> TMA store, and LSE = (m + log2 l) ln 2.
+//               share it, so the result is unchanged).  At the end O / l ->
+//               bf16 -> shared (the Q buffer of the tile, no longer read) -> TMA
+//               store, and LSE = (m + log2 l) ln 2.
 //
 // The launch is a list of items, one per (batch*head, 256-row query block),
 // on a 1-D grid.  Heads go in groups whose K and V fit in half of L2, one group
