@@ -272,13 +272,14 @@ def config_of(w):
             if io > 2 * L2_BYTES else "L2 flushed (256 MB write) before each timed step"}
 
 
-def launches_per_call(w, sms: int) -> int:
-    """Kernels one attn_fwd call launches.  bf16: the main kernel plus, when
-    some items go to split CTAs (all items of a grid filling at most half the
-    SMs; without the causal mask, also a last wave filling at most half of
-    them), the split-CTA kernel.  fp32: one kernel."""
+def kernels_per_call(w, sms: int) -> list:
+    """Kernels one attn_fwd call launches.  bf16: the main kernel for whole
+    waves of 256-row items, and the split-CTA kernel when some items go to
+    split CTAs (all items of a grid filling at most half the SMs; without the
+    causal mask, also a last wave filling at most half of them).  fp32: one
+    kernel."""
     if w.dtype != "bf16":
-        return 1
+        return [KERNEL_NAME["f32"]]
     n_items = w.B * w.H * ((w.N + 255) // 256)
     if 2 * n_items <= sms:
         n_split = n_items
@@ -286,7 +287,12 @@ def launches_per_call(w, sms: int) -> int:
         n_split = n_items % sms
     else:
         n_split = 0
-    return int(n_items - n_split > 0) + int(n_split > 0)
+    names = [KERNEL_NAME["bf16"]] if n_items - n_split > 0 else []
+    return names + (["attn_fwd_bf16_tc_split_kernel"] if n_split > 0 else [])
+
+
+def launches_per_call(w, sms: int) -> int:
+    return len(kernels_per_call(w, sms))
 
 
 EAGER_MAX_SCORE_BYTES = 64 << 30  # S alone; S and P together at most 128 GiB
@@ -449,7 +455,8 @@ def run_ours(args, w):
         traffic = profiled_traffic("bf16", w.name)
         roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
                     "unit": "TFLOP/s", "frac": kernel_tflops / peak, "traffic": traffic,
-                    "kernel": KERNEL_NAME["bf16"],
+                    "kernel": " + ".join(kernels_per_call(
+                        w, torch.cuda.get_device_properties(dev).multi_processor_count)),
                     "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} "
                                    "bf16 dense (MEASURED_PEAKS.json)",
                     "algorithmic_flops_per_launch": w.flops,
