@@ -85,11 +85,11 @@ def kernel_hash(dtype: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_value(dtype: str, workload: str, key: str):
+def profiled_value(dtype: str, workload: str, key: str, kernel: str = None):
     """A figure (``key: value`` line) from the committed ncu summary for this
-    kernel and workload, or None when there is none or the kernel changed
-    since it was captured."""
-    p = os.path.join(ROOT, "profiles", f"{KERNEL_NAME[dtype]}_{workload}.md")
+    kernel (by default the dtype's main kernel) and workload, or None when
+    there is none or the kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", f"{kernel or KERNEL_NAME[dtype]}_{workload}.md")
     if not os.path.exists(p):
         return None
     text = open(p).read()
@@ -100,9 +100,9 @@ def profiled_value(dtype: str, workload: str, key: str):
     return float(t.group(1))
 
 
-def profiled_traffic(dtype: str, workload: str):
+def profiled_traffic(dtype: str, workload: str, kernel: str = None):
     """DRAM bytes per launch (read + write) from the committed ncu summary."""
-    return profiled_value(dtype, workload, "traffic_bytes_per_launch")
+    return profiled_value(dtype, workload, "traffic_bytes_per_launch", kernel)
 
 
 class ClockSampler:
@@ -452,11 +452,13 @@ def run_ours(args, w):
     if w.dtype == "bf16":
         peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         kernel_tflops = w.flops / (statistics.mean(kernel_ms) * 1e-3) / 1e12
-        traffic = profiled_traffic("bf16", w.name)
+        kernels = kernels_per_call(w, torch.cuda.get_device_properties(dev).multi_processor_count)
+        # The traffic and tensor-pipe figures are those of the first (dominant)
+        # kernel's committed capture.
+        traffic = profiled_traffic("bf16", w.name, kernels[0])
         roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
                     "unit": "TFLOP/s", "frac": kernel_tflops / peak, "traffic": traffic,
-                    "kernel": " + ".join(kernels_per_call(
-                        w, torch.cuda.get_device_properties(dev).multi_processor_count)),
+                    "kernel": " + ".join(kernels),
                     "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} "
                                    "bf16 dense (MEASURED_PEAKS.json)",
                     "algorithmic_flops_per_launch": w.flops,
@@ -464,7 +466,7 @@ def run_ours(args, w):
                     # and the ncu tensor-pipe activity of the committed capture.
                     "frac_of_nominal_dense": kernel_tflops / NOMINAL_BF16_DENSE_TFLOPS,
                     "ncu_tensor_pipe_active_pct": profiled_value(
-                        "bf16", w.name, "tensor_pipe_active_pct")}
+                        "bf16", w.name, "tensor_pipe_active_pct", kernels[0])}
     else:
         kernel_tflops = w.flops / (statistics.mean(kernel_ms) * 1e-3) / 1e12
         # fp32 FMA pipe: 152 SMs x 128 lanes x 2 FLOP x max SM clock.
