@@ -95,6 +95,24 @@ def test_parity_main_kernel_and_tail(d, causal, B, H, N):
                  f"bf16 d={d} causal={causal} {B}x{H}x{N}")
 
 
+# All-split grids with long key loops: every item goes to the split kernel
+# (at most half as many items as SMs), and each of its query tiles walks 8 or
+# more key tiles, so its barriers go through many phases (ragged N included).
+SPLIT_LONG_SHAPES = [(1, 4, 4096), (2, 1, 3001)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", SPLIT_LONG_SHAPES)
+def test_parity_split_long_key_loops(d, causal, B, H, N):
+    q, k, v = make_qkv(B, H, N, d, seed=7000 + N + d + H, dtype="bf16")
+    scale = _scale(d)
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    assert_close("bf16", o, lse, o_ref, lse_ref, float(v.float().abs().max()),
+                 f"bf16 d={d} causal={causal} {B}x{H}x{N}")
+
+
 # Grids of two to three waves of 256-row items on the main kernel: CTAs of
 # one SM run items of different lengths (causal) one after the other, with
 # ragged last tiles, both head dims and items of different heads.
