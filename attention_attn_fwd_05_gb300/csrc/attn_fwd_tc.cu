@@ -589,10 +589,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     if (j < TA) issue_s(0, slot_addr(nK));
                     if (j >= 1) {
                         // O_B += P_B(j-1) V_{j-1}.
+                        // V_{j-1} was seen complete before O_A += P_A(j-1) V_{j-1}
+                        // (j - 1 < T_A inside this loop).
                         const int nV = 2 * (j - 1) + 1;
-                        if (!(ok = wait_full(nV) &&
-                                   spin_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl)))
-                            break;
+                        if (!(ok = spin_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl))) break;
                         tc_fence_after();
                         issue_pv(1, slot_addr(nV), j == 1);
                     }
@@ -608,8 +608,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     }
                 }
                 if (ok) {
+                    // V_{T_B-1} was seen before O_A's last product unless T_A < T_B.
                     const int j = TB - 1, nV = 2 * j + 1;
-                    ok = wait_full(nV) && spin_wait(bar(C::B_PFULL + 1), j & 1, ctl);
+                    ok = (j < TA || wait_full(nV)) && spin_wait(bar(C::B_PFULL + 1), j & 1, ctl);
                     if (ok) {
                         tc_fence_after();
                         issue_pv(1, slot_addr(nV), j == 0);
