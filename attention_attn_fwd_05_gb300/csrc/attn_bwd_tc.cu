@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // contiguous; the two 64-column halves BN*128 bytes apart).
             for (int t = 0; ok && t < T; ++t) {
                 const int s = t % NSTAGE;
-                if (!(ok = bounded_wait(bar(C::B_PFULL), t & 1, ctl))) break;
+                if (!(ok = spin_wait(bar(C::B_PFULL), t & 1, ctl))) break;
                 tc_fence_after();
                 gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_S, sdesc_sw128(sG(s), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     issue_s(t + 1);
                 }
-                if (!(ok = bounded_wait(bar(C::B_DSRDY), t & 1, ctl))) break;
+                if (!(ok = spin_wait(bar(C::B_DSRDY), t & 1, ctl))) break;
                 tc_fence_after();
                 gemm_ts_k8(tmem + C::TM_ACC1, tmem + C::TM_DP, sdesc_sw128(sQ(s), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
@@ -333,13 +333,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         // All four warps run every step (a failed wait only makes the rest
         // return at once), so the named barrier below always sees them all.
+        // This thread's query column of the next block is read from global
+        // memory one step ahead, so its latency hides behind a block's work.
+        auto col_vals = [&](int st_, float &nb_, float &dv_) {
+            const int qi = (q0 + st_) * BN + t;
+            nb_ = qi < N ? -lse_bh[qi] * LOG2E : -INFINITY;  // rows past N: P = 0
+            dv_ = qi < N ? -dl_bh[qi] : 0.f;                 // -D, for the packed dP - D
+        };
+        float nb_next = 0.f, dv_next = 0.f;
+        if (T > 0) col_vals(0, nb_next, dv_next);
         for (int st = 0; st < T; ++st) {
             const int qb = q0 + st;
             float *nb = vec + (st & 1) * 2 * BN;  // -LSE log2e per query column
             float *dv = nb + BN;                 // -D per query column
-            const int qi = qb * BN + t;
-            nb[t] = qi < N ? -lse_bh[qi] * LOG2E : -INFINITY;  // rows past N: P = 0
-            dv[t] = qi < N ? -dl_bh[qi] : 0.f;  // -D, for the packed dP - D
+            nb[t] = nb_next;
+            dv[t] = dv_next;
+            if (st + 1 < T) col_vals(st + 1, nb_next, dv_next);
             named_bar_sync(1, BM);
             ok = __all_sync(0xffffffffu, bounded_wait(bar(C::B_SFULL), st & 1, ctl)) && ok;
             tc_fence_after();
@@ -516,13 +525,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int s = t % NSTAGE;
                 bool s_next = false;
                 if (t + 1 < T) {
-                    if (!(ok = bounded_wait(bar(C::B_PFULL), t & 1, ctl))) break;  // S(t) read
+                    if (!(ok = spin_wait(bar(C::B_PFULL), t & 1, ctl))) break;  // S(t) read
                     if (mbar_test_wait(bar(C::B_FULL + (t + 1) % NSTAGE), ((t + 1) / NSTAGE) & 1)) {
                         issue_s(t + 1);
                         s_next = true;
                     }
                 }
-                if (!(ok = bounded_wait(bar(C::B_DSRDY), t & 1, ctl))) break;
+                if (!(ok = spin_wait(bar(C::B_DSRDY), t & 1, ctl))) break;
                 tc_fence_after();
                 gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_DP, sdesc_sw128(sK(s), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
