@@ -577,11 +577,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 mma_commit(drain);
                 drain_wait(drain, 0, timeout_ns);
             } else {
-                // Two S buffers (d = 128), one issuer for both tiles.  Each P V
-                // product waits first for its V tile (long landed, off the
+                // Two S buffers (d = 128), one issuer for both tiles.  Tile A's
+                // P V product waits first for its V tile (long landed, off the
                 // critical path) and then, spinning, for the softmax's P, so the
                 // issuer goes from "P is ready" straight to the MMAs (+0.5-3 %
-                // measured).
+                // measured); tile B's product with the same V tile one GEMM
+                // later only waits for its P.
                 bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl);
                 for (int j = 0; ok && j < TB; ++j) {
                     const int nK = 2 * j;
