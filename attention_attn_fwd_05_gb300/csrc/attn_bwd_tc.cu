@@ -14,8 +14,9 @@
 // each):
 //
 //   bwd_dkdv_tc_kernel   one CTA per 128-key block (keys on the TMEM lanes).
-//       K and V stay in shared memory; Q and dO blocks stream through a
-//       two-stage ring.  Per query block:
+//       K and V stay in shared memory; Q and dO blocks stream through a ring
+//       of block pairs (two stages at d = 128, three at d = 64).  Per query
+//       block:
 //         S^T = K Q^T,  dP^T = V dO^T                  (SS MMAs -> TMEM)
 //         P^T = exp2(S^T scale log2e - LSE log2e),  dS^T = P^T (dP^T - D)
 //                                                     (CUDA cores, bf16 -> TMEM)
@@ -47,7 +48,6 @@ namespace bwdtc {
 
 constexpr int BM = 128;            // rows of the block a CTA owns
 constexpr int BN = 128;            // rows of a streamed block
-constexpr int NSTAGE = 2;          // ring depth (streamed block pairs)
 constexpr int WARP_TMA = 4;
 constexpr int WARP_MMA = 5;
 constexpr int NUM_THREADS = 192;   // 4 row warps + TMA warp + MMA warp
@@ -57,19 +57,22 @@ constexpr float LOG2E = 1.44269504088896340736f;
 template <int D>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+    // Ring depth: two streamed block pairs at d = 128 (shared memory is full),
+    // more at d = 64.
+    static constexpr int NS = (D == 64) ? 3 : 2;
     static constexpr int DBLK = D / 64;                  // 128-byte column blocks per row
     static constexpr uint32_t TILE = BM * D * 2;          // one 128-row bf16 tile
     static constexpr uint32_t OFF_RES = 0;                // two resident tiles
-    static constexpr uint32_t OFF_RING = 2 * TILE;        // NSTAGE x two streamed tiles
-    static constexpr uint32_t OFF_VEC = OFF_RING + NSTAGE * 2 * TILE;  // [2 buf][2][BN] floats
+    static constexpr uint32_t OFF_RING = 2 * TILE;        // NS x two streamed tiles
+    static constexpr uint32_t OFF_VEC = OFF_RING + NS * 2 * TILE;  // [2 buf][2][BN] floats
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 2 * BN * 4;
     static constexpr uint32_t BAR_BYTES = 128;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + base alignment slack
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
     static constexpr int B_RES = 0;                  // resident tiles landed
-    static constexpr int B_FULL = 1;                 // [NSTAGE] streamed pair landed
-    static constexpr int B_EMPTY = B_FULL + NSTAGE;  // [NSTAGE] streamed pair consumed
-    static constexpr int B_SFULL = B_EMPTY + NSTAGE; // S in TMEM
+    static constexpr int B_FULL = 1;                 // [NS] streamed pair landed
+    static constexpr int B_EMPTY = B_FULL + NS;  // [NS] streamed pair consumed
+    static constexpr int B_SFULL = B_EMPTY + NS; // S in TMEM
     static constexpr int B_DPRDY = B_SFULL + 1;      // dP in TMEM
     static constexpr int B_PFULL = B_DPRDY + 1;      // P in TMEM (dK/dV kernel; one arrival per row)
     static constexpr int B_DSRDY = B_PFULL + 1;      // dS in TMEM (one arrival per row)
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_RES), 1);
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < C::NS; ++s) {
             mbar_init(bar(C::B_FULL + s), 1);
             mbar_init(bar(C::B_EMPTY + s), 1);
         }
@@ -248,9 +251,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             int t = 0;
             for (; t < T; ++t) {
-                const int s = t % NSTAGE;
-                if (t >= NSTAGE &&
-                    !bounded_wait(bar(C::B_EMPTY + s), ((t / NSTAGE) - 1) & 1, ctl))
+                const int s = t % C::NS;
+                if (t >= C::NS &&
+                    !bounded_wait(bar(C::B_EMPTY + s), ((t / C::NS) - 1) & 1, ctl))
                     break;
                 const int qr = (q0 + t) * BN;
                 mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
@@ -260,8 +263,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             drain_wait(bar(C::B_RES), 0, timeout_ns);
-            for (int i = (t > NSTAGE ? t - NSTAGE : 0); i < t; ++i)
-                drain_wait(bar(C::B_FULL + i % NSTAGE), (i / NSTAGE) & 1, timeout_ns);
+            for (int i = (t > C::NS ? t - C::NS : 0); i < t; ++i)
+                drain_wait(bar(C::B_FULL + i % C::NS), (i / C::NS) & 1, timeout_ns);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // K-major), each on its own barrier so the row warps start on P^T
             // while dP^T is still being computed.
             auto issue_s = [&](int t) {
-                const uint64_t b = sdesc_sw128(sQ(t % NSTAGE), 16, 1024);
+                const uint64_t b = sdesc_sw128(sQ(t % C::NS), 16, 1024);
                 if constexpr (D == 128)
                     gemm_ss_k8(tmem + C::TM_S, kdesc, b, idesc_s, 0u);
                 else
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mma_commit(bar(C::B_SFULL));
             };
             auto issue_dp = [&](int t) {
-                const uint64_t b = sdesc_sw128(sG(t % NSTAGE), 16, 1024);
+                const uint64_t b = sdesc_sw128(sG(t % C::NS), 16, 1024);
                 if constexpr (D == 128)
                     gemm_ss_k8(tmem + C::TM_DP, vdesc, b, idesc_s, 0u);
                 else
@@ -300,14 +303,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // comes from TMEM; B is the streamed tile read MN-major (d
             // contiguous; the two 64-column halves BN*128 bytes apart).
             for (int t = 0; ok && t < T; ++t) {
-                const int s = t % NSTAGE;
+                const int s = t % C::NS;
                 if (!(ok = spin_wait(bar(C::B_PFULL), t & 1, ctl))) break;
                 tc_fence_after();
                 gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_S, sdesc_sw128(sG(s), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
                 if (t + 1 < T) {
-                    if (!(ok = bounded_wait(bar(C::B_FULL + (t + 1) % NSTAGE),
-                                            ((t + 1) / NSTAGE) & 1, ctl)))
+                    if (!(ok = bounded_wait(bar(C::B_FULL + (t + 1) % C::NS),
+                                            ((t + 1) / C::NS) & 1, ctl)))
                         break;
                     issue_s(t + 1);
                 }
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_RES), 1);
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < C::NS; ++s) {
             mbar_init(bar(C::B_FULL + s), 1);
             mbar_init(bar(C::B_EMPTY + s), 1);
         }
@@ -475,9 +478,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             int t = 0;
             for (; t < T; ++t) {
-                const int s = t % NSTAGE;
-                if (t >= NSTAGE &&
-                    !bounded_wait(bar(C::B_EMPTY + s), ((t / NSTAGE) - 1) & 1, ctl))
+                const int s = t % C::NS;
+                if (t >= C::NS &&
+                    !bounded_wait(bar(C::B_EMPTY + s), ((t / C::NS) - 1) & 1, ctl))
                     break;
                 mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
                 for (int c = 0; c < C::DBLK; ++c) {
@@ -486,8 +489,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             drain_wait(bar(C::B_RES), 0, timeout_ns);
-            for (int i = (t > NSTAGE ? t - NSTAGE : 0); i < t; ++i)
-                drain_wait(bar(C::B_FULL + i % NSTAGE), (i / NSTAGE) & 1, timeout_ns);
+            for (int i = (t > C::NS ? t - C::NS : 0); i < t; ++i)
+                drain_wait(bar(C::B_FULL + i % C::NS), (i / C::NS) & 1, timeout_ns);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024), gdesc = sdesc_sw128(sG, 16, 1024);
             // S = Q K^T and dP = dO V^T of key block t, each on its own barrier.
             auto issue_s = [&](int t) {
-                const uint64_t b = sdesc_sw128(sK(t % NSTAGE), 16, 1024);
+                const uint64_t b = sdesc_sw128(sK(t % C::NS), 16, 1024);
                 if constexpr (D == 128)
                     gemm_ss_k8(tmem + C::TM_S, qdesc, b, idesc_s, 0u);
                 else
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mma_commit(bar(C::B_SFULL));
             };
             auto issue_dp = [&](int t) {
-                const uint64_t b = sdesc_sw128(sV(t % NSTAGE), 16, 1024);
+                const uint64_t b = sdesc_sw128(sV(t % C::NS), 16, 1024);
                 if constexpr (D == 128)
                     gemm_ss_k8(tmem + C::TM_DP, gdesc, b, idesc_s, 0u);
                 else
@@ -522,11 +525,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // dQ += dS K (A = dS from TMEM, B = the K tile read MN-major), then
             // dP of block t+1 (it overwrites dS, after dQ in issue order).
             for (int t = 0; ok && t < T; ++t) {
-                const int s = t % NSTAGE;
+                const int s = t % C::NS;
                 bool s_next = false;
                 if (t + 1 < T) {
                     if (!(ok = spin_wait(bar(C::B_PFULL), t & 1, ctl))) break;  // S(t) read
-                    if (mbar_test_wait(bar(C::B_FULL + (t + 1) % NSTAGE), ((t + 1) / NSTAGE) & 1)) {
+                    if (mbar_test_wait(bar(C::B_FULL + (t + 1) % C::NS), ((t + 1) / C::NS) & 1)) {
                         issue_s(t + 1);
                         s_next = true;
                     }
@@ -538,8 +541,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mma_commit(bar(C::B_EMPTY + s));
                 if (t + 1 < T) {
                     if (!s_next) {
-                        if (!(ok = bounded_wait(bar(C::B_FULL + (t + 1) % NSTAGE),
-                                                ((t + 1) / NSTAGE) & 1, ctl)))
+                        if (!(ok = bounded_wait(bar(C::B_FULL + (t + 1) % C::NS),
+                                                ((t + 1) / C::NS) & 1, ctl)))
                             break;
                         issue_s(t + 1);
                     }
