@@ -24,7 +24,8 @@
 //       issued as dV(t), S^T(t+1), dK(t), dP^T(t+1), so the row warps' work
 //       on block t overlaps dP^T(t), dV(t) and S^T(t+1).
 //   bwd_dq_tc_kernel     one CTA per 128-query block (queries on the lanes).
-//       Q and dO stay; K and V blocks stream.  Per key block:
+//       Q and dO stay; K and V blocks stream through rings of their own (three
+//       K slots, two V slots at d = 128, three at d = 64).  Per key block:
 //         S = Q K^T,  dP = dO V^T;  dS = P (dP - D);  dQ += dS K,
 //       with S of the next block issued as soon as the row warps have read S.
 //
@@ -83,6 +84,40 @@ struct Cfg {
     static_assert(8 * NUM_BARS + 8 <= BAR_BYTES, "barrier area too small");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget exceeded");
     static_assert(TM_ACC1 + D <= TMEM_COLS, "TMEM budget exceeded");
+};
+
+// The dQ kernel's shared memory: Q and dO resident, and K and V streamed
+// through rings of their own, KS slots for K (S of the next key block is
+// issued as soon as the row warps have read S, so its K is wanted early) and
+// VS for V.  A V slot comes back with the K slot of the same key block: dQ +=
+// dS K, whose completion frees that K slot, is issued after dP has read V.
+template <int D>
+struct DqCfg {
+    using C = Cfg<D>;
+    static constexpr int KS = 3;
+    static constexpr int VS = (D == 64) ? 3 : 2;
+    static constexpr int DBLK = C::DBLK;
+    static constexpr uint32_t TILE = C::TILE;
+    static constexpr uint32_t TM_S = C::TM_S, TM_DP = C::TM_DP, TM_ACC0 = C::TM_ACC0;
+    static constexpr uint32_t OFF_RES = 0;                     // Q, dO
+    static constexpr uint32_t OFF_K = 2 * TILE;                // KS K slots
+    static constexpr uint32_t OFF_V = OFF_K + KS * TILE;       // VS V slots
+    static constexpr uint32_t OFF_BAR = OFF_V + VS * TILE;
+    static constexpr int B_RES = 0;
+    static constexpr int B_FULLK = 1;                 // [KS] K slot landed
+    static constexpr int B_EMPTYK = B_FULLK + KS;     // [KS] K slot (and the V of that block) consumed
+    static constexpr int B_FULLV = B_EMPTYK + KS;     // [VS] V slot landed
+    static constexpr int B_SFULL = B_FULLV + VS;
+    static constexpr int B_DPRDY = B_SFULL + 1;
+    static constexpr int B_PFULL = B_DPRDY + 1;
+    static constexpr int B_DSRDY = B_PFULL + 1;
+    static constexpr int B_DONE = B_DSRDY + 1;
+    static constexpr int NUM_BARS = B_DONE + 1;
+    static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
+    static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+    static constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + base alignment slack
+    static_assert(VS <= KS, "a V slot is freed through the K ring");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget exceeded");
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
@@ -425,14 +460,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      const __grid_constant__ CUtensorMap tmDQ, const float *__restrict__ lse,
                      const float *__restrict__ delta, int N, float scale, int causal,
                      uint32_t *status, uint64_t timeout_ns) {
-    using C = Cfg<D>;
+    using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::OFF_RES, sG = sQ + C::TILE;
-    auto sK = [&](int s) -> uint32_t { return sbase + C::OFF_RING + (uint32_t)s * 2 * C::TILE; };
-    auto sV = [&](int s) -> uint32_t { return sK(s) + C::TILE; };
+    auto sK = [&](int s) -> uint32_t { return sbase + C::OFF_K + (uint32_t)s * C::TILE; };
+    auto sV = [&](int s) -> uint32_t { return sbase + C::OFF_V + (uint32_t)s * C::TILE; };
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM_SLOT);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_ABORT);
@@ -447,10 +482,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_RES), 1);
-        for (int s = 0; s < C::NS; ++s) {
-            mbar_init(bar(C::B_FULL + s), 1);
-            mbar_init(bar(C::B_EMPTY + s), 1);
+        for (int s = 0; s < C::KS; ++s) {
+            mbar_init(bar(C::B_FULLK + s), 1);
+            mbar_init(bar(C::B_EMPTYK + s), 1);
         }
+        for (int s = 0; s < C::VS; ++s) mbar_init(bar(C::B_FULLV + s), 1);
         mbar_init(bar(C::B_SFULL), 1);
         mbar_init(bar(C::B_DPRDY), 1);
         mbar_init(bar(C::B_PFULL), BM);
@@ -476,21 +512,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_load_3d(sQ + c * (BM * 128), &tmQ, c * 64, qb * BM, bh, bar(C::B_RES));
                 tma_load_3d(sG + c * (BM * 128), &tmG, c * 64, qb * BM, bh, bar(C::B_RES));
             }
-            int t = 0;
-            for (; t < T; ++t) {
-                const int s = t % C::NS;
-                if (t >= C::NS &&
-                    !bounded_wait(bar(C::B_EMPTY + s), ((t / C::NS) - 1) & 1, ctl))
+            int tk = 0, tv = 0;  // K and V loads issued
+            for (int t = 0; t < T; ++t) {
+                const int sk = t % C::KS, sv = t % C::VS;
+                if (t >= C::KS &&
+                    !bounded_wait(bar(C::B_EMPTYK + sk), ((t / C::KS) - 1) & 1, ctl))
                     break;
-                mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
-                for (int c = 0; c < C::DBLK; ++c) {
-                    tma_load_3d(sK(s) + c * (BN * 128), &tmK, c * 64, t * BN, bh, bar(C::B_FULL + s));
-                    tma_load_3d(sV(s) + c * (BN * 128), &tmV, c * 64, t * BN, bh, bar(C::B_FULL + s));
-                }
+                mbar_arrive_expect_tx(bar(C::B_FULLK + sk), C::TILE);
+                for (int c = 0; c < C::DBLK; ++c)
+                    tma_load_3d(sK(sk) + c * (BN * 128), &tmK, c * 64, t * BN, bh,
+                                bar(C::B_FULLK + sk));
+                tk = t + 1;
+                // The V slot held V(t - VS), read by dP(t - VS), which was
+                // issued before dQ(t - VS): that K slot's release frees it.
+                if (t >= C::VS && !bounded_wait(bar(C::B_EMPTYK + (t - C::VS) % C::KS),
+                                                ((t - C::VS) / C::KS) & 1, ctl))
+                    break;
+                mbar_arrive_expect_tx(bar(C::B_FULLV + sv), C::TILE);
+                for (int c = 0; c < C::DBLK; ++c)
+                    tma_load_3d(sV(sv) + c * (BN * 128), &tmV, c * 64, t * BN, bh,
+                                bar(C::B_FULLV + sv));
+                tv = t + 1;
             }
             drain_wait(bar(C::B_RES), 0, timeout_ns);
-            for (int i = (t > C::NS ? t - C::NS : 0); i < t; ++i)
-                drain_wait(bar(C::B_FULL + i % C::NS), (i / C::NS) & 1, timeout_ns);
+            for (int i = (tk > C::KS ? tk - C::KS : 0); i < tk; ++i)
+                drain_wait(bar(C::B_FULLK + i % C::KS), (i / C::KS) & 1, timeout_ns);
+            for (int i = (tv > C::VS ? tv - C::VS : 0); i < tv; ++i)
+                drain_wait(bar(C::B_FULLV + i % C::VS), (i / C::VS) & 1, timeout_ns);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -500,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024), gdesc = sdesc_sw128(sG, 16, 1024);
             // S = Q K^T and dP = dO V^T of key block t, each on its own barrier.
             auto issue_s = [&](int t) {
-                const uint64_t b = sdesc_sw128(sK(t % C::NS), 16, 1024);
+                const uint64_t b = sdesc_sw128(sK(t % C::KS), 16, 1024);
                 if constexpr (D == 128)
                     gemm_ss_k8(tmem + C::TM_S, qdesc, b, idesc_s, 0u);
                 else
@@ -508,44 +556,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mma_commit(bar(C::B_SFULL));
             };
             auto issue_dp = [&](int t) {
-                const uint64_t b = sdesc_sw128(sV(t % C::NS), 16, 1024);
+                const uint64_t b = sdesc_sw128(sV(t % C::VS), 16, 1024);
                 if constexpr (D == 128)
                     gemm_ss_k8(tmem + C::TM_DP, gdesc, b, idesc_s, 0u);
                 else
                     gemm_ss_k4(tmem + C::TM_DP, gdesc, b, idesc_s, 0u);
                 mma_commit(bar(C::B_DPRDY));
             };
-            bool ok = bounded_wait(bar(C::B_RES), 0, ctl) && bounded_wait(bar(C::B_FULL), 0, ctl);
-            if (ok) {
-                issue_s(0);
-                issue_dp(0);
-            }
+            auto full_k = [&](int t) {
+                return bounded_wait(bar(C::B_FULLK + t % C::KS), (t / C::KS) & 1, ctl);
+            };
+            auto full_v = [&](int t) {
+                return bounded_wait(bar(C::B_FULLV + t % C::VS), (t / C::VS) & 1, ctl);
+            };
+            bool ok = bounded_wait(bar(C::B_RES), 0, ctl) && full_k(0);
+            if (ok) issue_s(0);
+            if (ok && (ok = full_v(0))) issue_dp(0);
             // Per block t: S of block t+1 as soon as the row warps have read S
-            // and block t+1 has landed (if it has not landed yet, after dQ),
-            // dQ += dS K (A = dS from TMEM, B = the K tile read MN-major), then
-            // dP of block t+1 (it overwrites dS, after dQ in issue order).
+            // and K of block t+1 has landed (if it has not landed yet, after
+            // dQ), dQ += dS K (A = dS from TMEM, B = the K tile read MN-major),
+            // then dP of block t+1 (it overwrites dS, after dQ in issue order).
             for (int t = 0; ok && t < T; ++t) {
-                const int s = t % C::NS;
+                const int sk = t % C::KS;
                 bool s_next = false;
                 if (t + 1 < T) {
                     if (!(ok = spin_wait(bar(C::B_PFULL), t & 1, ctl))) break;  // S(t) read
-                    if (mbar_test_wait(bar(C::B_FULL + (t + 1) % C::NS), ((t + 1) / C::NS) & 1)) {
+                    tc_fence_after();
+                    if (mbar_test_wait(bar(C::B_FULLK + (t + 1) % C::KS), ((t + 1) / C::KS) & 1)) {
                         issue_s(t + 1);
                         s_next = true;
                     }
                 }
                 if (!(ok = spin_wait(bar(C::B_DSRDY), t & 1, ctl))) break;
                 tc_fence_after();
-                gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_DP, sdesc_sw128(sK(s), BN * 128, 1024),
+                gemm_ts_k8(tmem + C::TM_ACC0, tmem + C::TM_DP, sdesc_sw128(sK(sk), BN * 128, 1024),
                            idesc_o, t > 0 ? 1u : 0u);
-                mma_commit(bar(C::B_EMPTY + s));
+                mma_commit(bar(C::B_EMPTYK + sk));
                 if (t + 1 < T) {
                     if (!s_next) {
-                        if (!(ok = bounded_wait(bar(C::B_FULL + (t + 1) % C::NS),
-                                                ((t + 1) / C::NS) & 1, ctl)))
-                            break;
+                        if (!(ok = full_k(t + 1))) break;
                         issue_s(t + 1);
                     }
+                    if (!(ok = full_v(t + 1))) break;
                     issue_dp(t + 1);
                 }
             }
@@ -635,7 +687,7 @@ static attn_status launch(const void *q, const void *k, const void *v, const voi
                      ATTN_ERR_CUDA) != ATTN_OK ||
         check_launch(cudaFuncSetAttribute(bwd_dq_tc_kernel<D>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)C::SMEM_BYTES),
+                                          (int)DqCfg<D>::SMEM_BYTES),
                      ATTN_ERR_CUDA) != ATTN_OK)
         return ATTN_ERR_CUDA;
     const dim3 grid((unsigned)BH, (unsigned)((N + BM - 1) / BM));
@@ -649,7 +701,7 @@ static attn_status launch(const void *q, const void *k, const void *v, const voi
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.dynamicSmemBytes = DqCfg<D>::SMEM_BYTES;
     cfg.stream = ctx.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
