@@ -55,11 +55,13 @@ constexpr int NUM_THREADS = 192;   // 4 row warps + TMA warp + MMA warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.44269504088896340736f;
 
+// TMEM columns of both kernels, and the dK/dV kernel's shared memory (the dQ
+// kernel's is DqCfg below).
 template <int D>
 struct Cfg {
     static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
     // Ring depth: two streamed block pairs at d = 128 (shared memory is full),
-    // more at d = 64.
+    // three at d = 64.
     static constexpr int NS = (D == 64) ? 3 : 2;
     static constexpr int DBLK = D / 64;                  // 128-byte column blocks per row
     static constexpr uint32_t TILE = BM * D * 2;          // one 128-row bf16 tile
