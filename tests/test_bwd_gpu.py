@@ -95,3 +95,28 @@ def test_bwd_parity_bf16_multiblock(d, causal, N, dist):
     _check("bf16", dq, rq, "dQ", scale * mx(k) * ds_bound)
     _check("bf16", dk, rk, "dK", scale * mx(q) * ds_bound)
     _check("bf16", dv, rv, "dV", mx(g))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [2000, 2561])
+def test_bwd_parity_bf16_long_rings(d, causal, N):
+    """bf16 backward over 16-21 streamed blocks per CTA, so every slot of the
+    streamed rings (K/V in the dQ kernel, Q/dO pairs in the dK/dV kernel) is
+    reused several times through both phases of its barriers; ragged tails."""
+    q, k, v = make_qkv(1, 2, N, d, seed=1300 + N + d, dtype="bf16")
+    scale = float(torch.tensor(1 / math.sqrt(d), dtype=torch.float32))
+    o64, lse64 = oracle.attn_fwd(q, k, v, scale, causal)
+    o = torch.from_numpy(o64).to(torch.bfloat16)
+    lse = torch.from_numpy(lse64).float()
+    g = torch.randn(q.shape, generator=torch.Generator().manual_seed(N + 7)).to(torch.bfloat16)
+    dq, dk, dv = attn_bwd(q.cuda(), k.cuda(), v.cuda(), o.cuda(), lse.cuda(), g.cuda(), scale,
+                          causal)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    rq, rk, rv = oracle.attn_bwd(q, k, v, o, g, lse, scale, causal)
+    mx = lambda t: float(t.float().abs().max())
+    ds_bound = 2 * mx(g) * mx(v)
+    _check("bf16", dq, rq, "dQ", scale * mx(k) * ds_bound)
+    _check("bf16", dk, rk, "dK", scale * mx(q) * ds_bound)
+    _check("bf16", dv, rv, "dV", mx(g))
