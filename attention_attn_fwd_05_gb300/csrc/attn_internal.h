@@ -64,9 +64,10 @@ attn_status launch_wait_selftest(const LaunchCtx &ctx);
 attn_status check_launch(cudaError_t e, attn_status on_error);
 
 // Largest N the bf16 path accepts.  The kernels' grids are 1-D (the items
-// are counted by the B*H*ceil(N/256) < 2^31 rule of check_fwd_shape); this
-// cap on N itself is kept from the first release so the documented limit
-// does not change.
+// are counted by the B*H*ceil(N/256) < 2^31 rule of check_fwd_shape) and
+// their row and key indices are 32-bit, so no index limit binds below 2^31;
+// the cap is a tested-range limit (GPU parity reaches N = 131072 on sampled
+// rows; a host test checks the rejection just above the cap).
 constexpr int64_t kMaxNBf16 = 65535LL * 128;
 
 // Shape, dtype and head-dim rules of attn_fwd (ATTN_OK or the error code),

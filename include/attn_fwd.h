@@ -70,9 +70,10 @@ typedef enum attn_dtype {
  *   lse      [B,H,N] fp32 output, natural-log log-sum-exp of the scaled
  *            logits of each row (device, fully overwritten), or NULL to skip.
  *   B, H, N  batch, heads, sequence length; each >= 1, N < 2^31 and
- *            B*H*N*d < 2^62.  ATTN_BF16 also needs N <= 8388480 (65535*128)
- *            and B*H*ceil(N/256) < 2^31 (the kernels' 1-D grid of
- *            256-row items); ATTN_F32 needs B*H <= 65535.
+ *            B*H*N*d < 2^62.  ATTN_BF16 also needs N <= 8388480 (65535*128,
+ *            a tested-range cap, not an index limit) and
+ *            B*H*ceil(N/256) < 2^31 (the kernels' 1-D grid of 256-row
+ *            items); ATTN_F32 needs B*H <= 65535.
  *   d        head dimension: 64 or 128.
  *   scale    multiplier applied to Q.K before the softmax (1/sqrt(d) usually).
  *            Any finite value with |scale| <= 2e38: positive, negative (the
