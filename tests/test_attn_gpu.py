@@ -353,6 +353,18 @@ def test_parity_many_heads(dtype):
     assert_close(dtype, o, lse, o_ref, lse_ref, float(v.float().abs().max()), f"{dtype} B*H=4096")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_parity_heads_beyond_65535_bf16(causal):
+    """B*H = 70000 heads of 3 rows (bf16): item indices of the kernels' 1-D grid
+    past 65535, against the oracle on every row.  (The exact-fp32 path keeps
+    B*H <= 65535.)"""
+    q, k, v = make_qkv(7, 10000, 3, 64, seed=93, dtype="bf16")
+    scale = _scale(64)
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    assert_close("bf16", o, lse, o_ref, lse_ref, float(v.float().abs().max()), "B*H=70000")
+
+
 # --------------------------------------------------- GPU invariances ---
 
 def test_t3g_key_shift_on_gpu():
