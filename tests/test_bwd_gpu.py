@@ -120,3 +120,29 @@ def test_bwd_parity_bf16_long_rings(d, causal, N):
     _check("bf16", dq, rq, "dQ", scale * mx(k) * ds_bound)
     _check("bf16", dk, rk, "dK", scale * mx(q) * ds_bound)
     _check("bf16", dv, rv, "dV", mx(g))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 1.0])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_parity_scales(dtype, scale, d, causal):
+    """Scales other than 1/sqrt(d) (the entry point accepts any finite one):
+    negative, zero (dQ and dK vanish exactly, dV is the mean of dO over the
+    visible queries) and 1 (peaked rows)."""
+    q, k, v = make_qkv(1, 2, 300, d, seed=1700 + d, dtype=dtype)
+    scale = float(torch.tensor(scale, dtype=torch.float32))
+    o64, lse64 = oracle.attn_fwd(q, k, v, scale, causal)
+    o = torch.from_numpy(o64).to(torch_dtype(dtype))
+    lse = torch.from_numpy(lse64).float()
+    g = torch.randn(q.shape, generator=torch.Generator().manual_seed(d + 3)).to(torch_dtype(dtype))
+    dq, dk, dv = attn_bwd(q.cuda(), k.cuda(), v.cuda(), o.cuda(), lse.cuda(), g.cuda(), scale,
+                          causal)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    rq, rk, rv = oracle.attn_bwd(q, k, v, o, g, lse, scale, causal)
+    mx = lambda t: float(t.float().abs().max())
+    ds_bound = 2 * mx(g) * mx(v)
+    _check(dtype, dq, rq, "dQ", abs(scale) * mx(k) * ds_bound)
+    _check(dtype, dk, rk, "dK", abs(scale) * mx(q) * ds_bound)
+    _check(dtype, dv, rv, "dV", mx(g))
