@@ -583,29 +583,46 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 // issuer goes from "P is ready" straight to the MMAs (+0.5-3 %
                 // measured); tile B's product with the same V tile one GEMM
                 // later only waits for its P.
-                bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl);
-                for (int j = 0; ok && j < TB; ++j) {
+                // Key tile 0, then the steady state with no run-time choices
+                // (key tiles 1 .. T_A - 1), then tile B's extra key tile
+                // (causal, T_B = T_A + 1) and its last product.
+                bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl) && wait_full(0);
+                if (ok) {
+                    issue_s(0, slot_addr(0));
+                    ok = bounded_wait(bar(C::B_Q + 1), 0, ctl);
+                }
+                if (ok) {
+                    issue_s(1, slot_addr(0));
+                    ok = wait_full(1) && spin_wait(bar(C::B_PFULL + 0), 0, ctl);
+                }
+                if (ok) {
+                    tc_fence_after();
+                    issue_pv(0, slot_addr(1), true);
+                }
+                for (int j = 1; ok && j < TA; ++j) {
                     const int nK = 2 * j;
                     if (!(ok = wait_full(nK))) break;
-                    if (j < TA) issue_s(0, slot_addr(nK));
-                    if (j >= 1) {
-                        // O_B += P_B(j-1) V_{j-1}.
-                        // V_{j-1} was seen complete before O_A += P_A(j-1) V_{j-1}
-                        // (j - 1 < T_A inside this loop).
-                        const int nV = 2 * (j - 1) + 1;
-                        if (!(ok = spin_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl))) break;
-                        tc_fence_after();
-                        issue_pv(1, slot_addr(nV), j == 1);
-                    }
-                    if (j == 0 && !(ok = bounded_wait(bar(C::B_Q + 1), 0, ctl))) break;
+                    issue_s(0, slot_addr(nK));
+                    // O_B += P_B(j-1) V_{j-1}; V_{j-1} was seen complete before
+                    // O_A += P_A(j-1) V_{j-1}.
+                    if (!(ok = spin_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl))) break;
+                    tc_fence_after();
+                    issue_pv(1, slot_addr(nK - 1), j == 1);
                     issue_s(1, slot_addr(nK));
-                    if (j < TA) {
-                        const int nV = 2 * j + 1;
-                        if (!(ok = wait_full(nV) && spin_wait(bar(C::B_PFULL + 0), j & 1, ctl)))
-                            break;
+                    if (!(ok = wait_full(nK + 1) && spin_wait(bar(C::B_PFULL + 0), j & 1, ctl)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(0, slot_addr(nK + 1), false);
+                }
+                if (ok) mma_commit(bar(C::B_ODONE + 0));
+                if (ok && TB > TA) {
+                    // Tile B's key tile T_A (causal): O_B += P_B(T_A - 1) V, S_B(T_A).
+                    const int nK = 2 * TA;
+                    ok = wait_full(nK) && spin_wait(bar(C::B_PFULL + 1), (TA - 1) & 1, ctl);
+                    if (ok) {
                         tc_fence_after();
-                        issue_pv(0, slot_addr(nV), j == 0);
-                        if (j == TA - 1) mma_commit(bar(C::B_ODONE + 0));
+                        issue_pv(1, slot_addr(nK - 1), TA == 1);
+                        issue_s(1, slot_addr(nK));
                     }
                 }
                 if (ok) {
