@@ -584,8 +584,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 // measured); tile B's product with the same V tile one GEMM
                 // later only waits for its P.
                 // Key tile 0, then the steady state with no run-time choices
-                // (key tiles 1 .. T_A - 1), then tile B's extra key tile
-                // (causal, T_B = T_A + 1) and its last product.
+                // (key tiles 1 .. T_A - 1: whole groups of NSLOT tiles with
+                // constant ring positions, then the remainder), then tile B's
+                // extra key tile (causal, T_B = T_A + 1) and its last product.
                 bool ok = bounded_wait(bar(C::B_Q + 0), 0, ctl) && wait_full(0);
                 if (ok) {
                     issue_s(0, slot_addr(0));
@@ -599,7 +600,34 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     tc_fence_after();
                     issue_pv(0, slot_addr(1), true);
                 }
-                for (int j = 1; ok && j < TA; ++j) {
+                // Steady state in groups of NSLOT key tiles: tile 1 + NSLOT g + i
+                // loads K into slot (2 + 2 i) % NSLOT and V into the next one,
+                // with phases that depend on i alone (2 NSLOT loads per group
+                // are an even number of ring turns), so inside a group every
+                // slot address and barrier phase is a constant.
+                constexpr int NS = C::NSLOT;
+                const int groups = (TA - 1) / NS;
+                for (int g = 0; ok && g < groups; ++g) {
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) {
+                        const int j = 1 + NS * g + i;
+                        const int sk = (2 + 2 * i) % NS, pk = ((2 + 2 * i) / NS) & 1;
+                        const int sv = (3 + 2 * i) % NS, pv = ((3 + 2 * i) / NS) & 1;
+                        const int sp = (1 + 2 * i) % NS;  // V_{j-1}
+                        if (!(ok = bounded_wait(bar(C::B_FULL + sk), (uint32_t)pk, ctl))) break;
+                        issue_s(0, sKV + (uint32_t)sk * C::SLOT_BYTES);
+                        if (!(ok = spin_wait(bar(C::B_PFULL + 1), (j - 1) & 1, ctl))) break;
+                        tc_fence_after();
+                        issue_pv(1, sKV + (uint32_t)sp * C::SLOT_BYTES, j == 1);
+                        issue_s(1, sKV + (uint32_t)sk * C::SLOT_BYTES);
+                        if (!(ok = bounded_wait(bar(C::B_FULL + sv), (uint32_t)pv, ctl) &&
+                                   spin_wait(bar(C::B_PFULL + 0), j & 1, ctl)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(0, sKV + (uint32_t)sv * C::SLOT_BYTES, false);
+                    }
+                }
+                for (int j = 1 + NS * groups; ok && j < TA; ++j) {
                     const int nK = 2 * j;
                     if (!(ok = wait_full(nK))) break;
                     issue_s(0, slot_addr(nK));
